@@ -1,0 +1,375 @@
+"""Benchmark of the blockwise ring-attention hot path on GB300.
+
+One step = the whole path over one batch of seeded synthetic input:
+RoPE of Q and K (rope_apply x 2) and the fused Ring-Attention kernel
+(ring_attn_fwd, P emulated ranks) on the rotated copies, all through the C ABI.
+Default workload: long-context causal prefill, B=1, H=32, T=65536, d=128, bf16,
+RoPE base 10000, P=16 zigzag ranks (the largest single-GPU workload).
+
+Prints ONE JSON line (rank 0).  `value` is attention TFLOP/s counting 4*d FLOP
+per visible (query, key) pair only, over the device-timed step with inputs
+resident in HBM (inputs of 1.6 GB exceed the 129 MB L2, so no flush is
+needed between steps).  `e2e` is the same metric through ring_attn_fwd with
+host buffers: pinned host->device copies of Q, K, V and device->host copies of
+out and lse inside the timed region.  `--impl reference` times the CPU oracle
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "attention TFLOP/s (visible pairs) and % of GB300 BF16 tensor peak; tokens/s"
+DEFAULT_WORKLOAD = "zigzag_prefill_64k_rope"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def visible_pairs(w, inp) -> int:
+    """Exact count of visible (query, key) pairs over all (b, h)."""
+    if w.pad_len is None and w.band is None:
+        per = w.T * (w.T + 1) // 2 if w.causal else w.T * w.T
+        return per * w.B * w.H
+    total = 0
+    T = w.T
+    dev = inp.q.device
+    i = torch.arange(T, device=dev).view(-1, 1)
+    j = torch.arange(T, device=dev).view(1, -1)
+    base = torch.ones((T, T), dtype=torch.bool, device=dev)
+    if w.causal:
+        base &= j <= i
+    if inp.am is not None:
+        base &= inp.am == 0
+    for b in range(w.B):
+        m = base
+        if inp.kpm is not None:
+            m = m & (inp.kpm[b] == 0).view(1, -1)
+        total += int(m.sum().item())
+    return total * w.H
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200", "-i", uuid], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                mhz.append(float(s[1].split()[0]))
+                mx = float(s[2].split()[0])
+                for n, v in zip(names, s[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def oracle_cpu_baseline(w, inp_cpu_head, seconds):
+    """Time the oracle, as it stands, on sampled query rows of one head (each
+    row over its full causal key range), RoPE included.  Returns the JSON
+    object for `cpu_baseline`."""
+    import oracle
+    q, k, v = inp_cpu_head            # (1, 1, T, d) float32 tensors on the CPU
+    T, d = w.T, w.d
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(0)
+
+    def run(nrows):
+        rows = np.sort(rng.choice(T, size=nrows, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        if w.rope_base is not None:
+            qr = oracle.rope(q, base=w.rope_base, round_to=w.dtype)
+            kr = oracle.rope(k, base=w.rope_base, round_to=w.dtype)
+        else:
+            qr, kr = q, k
+        oracle.attention(qr, kr, v, causal=w.causal, rows=rows, nthreads=threads)
+        dt = time.perf_counter() - t0
+        pairs = int((rows + 1).sum()) if w.causal else nrows * T
+        return dt, pairs
+
+    dt, pairs = run(threads)
+    rate = pairs / max(dt, 1e-6)
+    n = int(min(T, max(threads, threads * round(seconds * rate / (T / 2) / threads))))
+    dt, pairs = run(n)
+    flops = 4.0 * d * pairs
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random query rows of one head (b=0, h=0) of {w.name}, each over its full "
+                      f"causal key range, RoPE of that head's Q and K included; {pairs} visible pairs "
+                      f"in {dt:.2f} s"}
+
+
+def reference_arm(args, w, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    g = torch.Generator().manual_seed(1000 + w.index)
+    shape = (1, 1, w.T, w.d)
+    qkv = []
+    for _ in range(3):
+        x = torch.randn(shape, generator=g) * w.std
+        qkv.append(x.to(w.torch_dtype).float())
+    times, last = [], None
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        last = oracle_cpu_baseline(w, qkv, seconds=max(2.0, args.cpu_seconds / 2))
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    value = last["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                                            "P": w.P, "partition": w.partition, "causal": w.causal,
+                                            "rope_base": w.rope_base},
+            "cpu_baseline": {k: last[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def native_arm(args, w, rank, world, local_rank):
+    import blockwise_attention_gb300 as ba
+    from blockwise_attention_gb300.workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    inp = make_inputs(w, dev)
+    rope = w.rope_base is not None
+    pairs = visible_pairs(w, inp)
+    flops = 4.0 * w.d * pairs
+    stream = torch.cuda.current_stream(dev)
+
+    qr = torch.empty_like(inp.q)
+    kr = torch.empty_like(inp.k)
+    out = torch.empty_like(inp.q)
+    lse = torch.empty(inp.q.shape[:3], dtype=torch.float32, device=dev)
+    ws_need = ba.ring_attn_fwd_workspace_size(w.B, w.H, w.T, w.d, inp.q.dtype, w.P, w.partition, args.mode,
+                                              inp.kpm is not None or inp.am is not None, False)
+    ws = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        if rope:
+            ba.rope_apply(inp.q, base=w.rope_base, out=qr)
+            ba.rope_apply(inp.k, base=w.rope_base, out=kr)
+            q_in, k_in = qr, kr
+        else:
+            q_in, k_in = inp.q, inp.k
+        if evs:
+            evs[1].record(stream)
+        ba.ring_attn_fwd(q_in, k_in, inp.v, P=w.P, partition=w.partition, mode=args.mode,
+                         key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, out=out, lse=lse,
+                         workspace=ws)
+        if evs:
+            evs[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = ba.sync_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
+    rope_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    kernels_per_step = (2 if rope else 0) + (1 if args.mode == "fused" else w.P) + \
+        (1 if (inp.kpm is not None or inp.am is not None) else 0)
+
+    # end to end through the one-call API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh = inp.q.cpu().pin_memory()
+        kh = inp.k.cpu().pin_memory()
+        vh = inp.v.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        qd, kd, vd = torch.empty_like(inp.q), torch.empty_like(inp.k), torch.empty_like(inp.v)
+        ws_e = ba.ring_attn_fwd_workspace_size(w.B, w.H, w.T, w.d, inp.q.dtype, w.P, w.partition, args.mode,
+                                               inp.kpm is not None or inp.am is not None, rope)
+        wse = torch.empty(max(ws_e, 1), dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            ba.ring_attn_fwd(qd, kd, vd, P=w.P, partition=w.partition, mode=args.mode,
+                             key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, rope=rope,
+                             rope_base=w.rope_base or 10000.0, out=out, lse=lse, workspace=wse)
+            oh.copy_(out, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = a.elapsed_time(b) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+        d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+        del qh, kh, vh, qd, kd, vd, wse
+
+    if ba.sync_status() != 0:
+        raise RuntimeError("device status error after the timed region")
+    if rank != 0:
+        return
+
+    peaks, peak_src = load_peaks()
+    attn_avg = statistics.mean(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": None, "kernel": "attn_tc_kernel<128>",
+            "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a repeated step)",
+            "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"]),
+            "kernel_ms": attn_avg}
+    cpu = None
+    if not args.no_cpu and world == 1 or (not args.no_cpu and rank == 0 and world == 1):
+        head = (inp.q[0:1, 0:1].float().cpu(), inp.k[0:1, 0:1].float().cpu(), inp.v[0:1, 0:1].float().cpu())
+        cpu = oracle_cpu_baseline(w, head, args.cpu_seconds)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": w.P,
+                       "partition": w.partition, "causal": w.causal, "rope_base": w.rope_base,
+                       "mode": args.mode, "visible_pairs": pairs, "flops_per_step": flops,
+                       "l2": "inputs (Q, K, V: 1.6 GB) larger than the 129 MB L2; no flush"},
+            "tokens_per_s": world * w.B * w.T / (ms_step * 1e-3),
+            "pct_of_bf16_peak": 100.0 * value / peak,
+            "rope_ms": statistics.mean(rope_ms),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": kernels_per_step * args.steps}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from blockwise_attention_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, w, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    try:
+        native_arm(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,306 @@
+"""Build and load libblockattn.so (CUDA, sm_103a) and bind its C ABI.
+
+The binding only marshals arguments: torch tensors become device pointers and
+element strides, outputs and workspace are allocated with torch, and every
+step of the computation runs in the library's kernels.  There is no other
+implementation behind these functions; if the library cannot be built or
+loaded they raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_CSRC = os.path.join(_PKG, "csrc")
+_BUILD = os.path.join(_PKG, "_build")
+LIB_PATH = os.path.join(_BUILD, "libblockattn.so")
+_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu"]
+_HEADERS = ["common.cuh", "internal.h", "epilogue.cuh"]
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+BA_OK, BA_ERR_ARG, BA_ERR_SHAPE, BA_ERR_CUDA, BA_ERR_TIMEOUT, BA_ERR_UNSUPPORTED, BA_ERR_WORKSPACE = \
+    0, -1, -2, -3, -4, -5, -6
+BA_F32, BA_BF16 = 0, 1
+PARTITIONS = {"contiguous": 0, "zigzag": 1}
+MODES = {"stepwise": 0, "fused": 1}
+BA_TILE_EMPTY, BA_TILE_FULL, BA_TILE_PARTIAL = 0, 1, 2
+
+_lib = None
+
+
+class BlockAttnError(RuntimeError):
+    def __init__(self, fn, code):
+        msg = _lib.ba_strerror(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{fn} failed: {msg} ({code})")
+        self.code = code
+
+
+def _nvcc():
+    for c in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
+        if c and (os.path.isabs(c) and os.path.exists(c) or not os.path.isabs(c)):
+            return c
+    return "nvcc"
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS]
+    deps.append(os.path.join(_ROOT, "include", "blockattn.h"))
+    return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA sources for sm_103a (in parallel) and link the shared library."""
+    if not force and not _stale():
+        return LIB_PATH
+    os.makedirs(_BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    common = [nvcc, *ARCH_FLAGS, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+              "-I", os.path.join(_ROOT, "include")]
+
+    def compile_one(src):
+        obj = os.path.join(_BUILD, src.replace(".cu", ".o"))
+        cmd = common + ["-c", os.path.join(_CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
+        if verbose and r.stderr:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(len(_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, _SOURCES))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class ba_tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("sB", ctypes.c_int64), ("sH", ctypes.c_int64),
+                ("sT", ctypes.c_int64)]
+
+
+EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ring_attn_fwd",
+            "ring_attn_fwd_workspace_size", "rope_apply", "ba_tile_classes", "ba_index_maps",
+            "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror"]
+
+
+def load(path: str | None = None):
+    """Load the library (building it first when needed) and declare signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = build()
+    lib = ctypes.CDLL(path)
+    i, i64, sz, vp, f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+    T = ba_tensor
+    lib.ba_strerror.restype = ctypes.c_char_p
+    lib.ba_strerror.argtypes = [i]
+    lib.attn_block_fwd_workspace_size.restype = sz
+    lib.attn_block_fwd_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_block_fwd.restype = i
+    lib.attn_block_fwd.argtypes = [T, T, T, i, i, i, i, i, i, i64, i64, vp, i64, vp, i64, i, f, vp, i, vp, i,
+                                   vp, sz, vp]
+    lib.attn_merge.restype = i
+    lib.attn_merge.argtypes = [vp, vp, vp, vp, i64, i, vp]
+    lib.ring_attn_fwd_workspace_size.restype = sz
+    lib.ring_attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, i, i]
+    lib.ring_attn_fwd.restype = i
+    lib.ring_attn_fwd.argtypes = [T, T, T, i, i, i, i, i, i, i, i, vp, i64, vp, i64, i, f, i, f, vp, i, vp, vp,
+                                  vp, sz, vp]
+    lib.rope_apply.restype = i
+    lib.rope_apply.argtypes = [T, i, i, i, i, i, vp, f, vp, vp]
+    lib.ba_tile_classes.restype = i
+    lib.ba_tile_classes.argtypes = [i, i, i, i64, i64, vp, i64, vp, i64, i, vp, vp]
+    lib.ba_index_maps.restype = i
+    lib.ba_index_maps.argtypes = [i, i, i, vp, vp]
+    lib.ba_sync_status.restype = i
+    lib.ba_sync_status.argtypes = [vp]
+    lib.ba_debug_wait_timeout.restype = i
+    lib.ba_debug_wait_timeout.argtypes = [i64, vp]
+    _lib = lib
+    return lib
+
+
+def _check(fn, rc):
+    if rc != BA_OK:
+        raise BlockAttnError(fn, rc)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return BA_F32
+    if t == torch.bfloat16:
+        return BA_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _tensor(x: torch.Tensor) -> ba_tensor:
+    if x.dim() != 4 or x.stride(-1) != 1:
+        raise ValueError("expected a (B, H, T, d) tensor with a contiguous last axis")
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return ba_tensor(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2))
+
+
+def _mask(m):
+    if m is None:
+        return None, 0
+    if m.dtype != torch.uint8 or m.dim() != 2 or m.stride(1) != 1 or not m.is_cuda:
+        raise ValueError("masks are 2-D uint8 CUDA tensors with a contiguous last axis")
+    return ctypes.c_void_p(m.data_ptr()), m.stride(0)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def attn_block_fwd(q, k, v, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None, causal=False,
+                   scale=None, out=None, out_dtype=None, lse=None, accumulate=False, workspace=None,
+                   stream=None):
+    """One attention block with per-row natural-log LSE; see include/blockattn.h."""
+    lib = load()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    dt = _dtype_code(q.dtype)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else q.dtype
+    if out is None:
+        out = torch.empty((B, H, Lq, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    need = lib.attn_block_fwd_workspace_size(B, Lq, Lk, int(kpm is not None or am is not None))
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib.attn_block_fwd(_tensor(q), _tensor(k), _tensor(v), B, H, Lq, Lk, d, dt, q_off, k_off, kpm, kpm_ld,
+                            am, am_ld, int(bool(causal)), 0.0 if scale is None else float(scale),
+                            _ptr(out), _dtype_code(out.dtype), _ptr(lse), int(bool(accumulate)),
+                            _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("attn_block_fwd", rc)
+    return out, lse
+
+
+def attn_merge(out_a, lse_a, out_b, lse_b, stream=None):
+    """In place: (out_a, lse_a) <- LSE merge of (out_a, lse_a) and (out_b, lse_b)."""
+    lib = load()
+    for t in (out_a, lse_a, out_b, lse_b):
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("attn_merge takes contiguous fp32 CUDA tensors")
+    d = out_a.shape[-1]
+    rows = lse_a.numel()
+    if out_a.numel() != rows * d or out_b.numel() != rows * d or lse_b.numel() != rows:
+        raise ValueError("shape mismatch")
+    _check("attn_merge", lib.attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), rows, d,
+                                        _stream(stream)))
+    return out_a, lse_a
+
+
+def ring_attn_fwd_workspace_size(B, H, T, d, dtype, P, partition="contiguous", mode="fused", has_masks=False,
+                                 rope=False, out_dtype=None):
+    lib = load()
+    dt = _dtype_code(dtype)
+    odt = dt if out_dtype is None else _dtype_code(out_dtype)
+    return lib.ring_attn_fwd_workspace_size(B, H, T, d, dt, P, PARTITIONS[partition], MODES[mode],
+                                            int(bool(has_masks)), int(bool(rope)), odt)
+
+
+def ring_attn_fwd(q, k, v, *, P, partition="contiguous", mode="fused", key_padding_mask=None, attn_mask=None,
+                  causal=False, scale=None, rope=False, rope_base=10000.0, out=None, out_dtype=None, lse=None,
+                  return_index_maps=False, workspace=None, stream=None):
+    """Ring Attention over P emulated ranks; see include/blockattn.h.
+    Returns (out, lse) or (out, lse, tok_of (P, T/P), schedule (P, P))."""
+    lib = load()
+    B, H, T, d = q.shape
+    dt = _dtype_code(q.dtype)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else q.dtype
+    if out is None:
+        out = torch.empty((B, H, T, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    masks = kpm is not None or am is not None
+    need = ring_attn_fwd_workspace_size(B, H, T, d, q.dtype, P, partition, mode, masks, rope, out.dtype)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    maps = None
+    if return_index_maps:
+        maps = (ctypes.c_int32 * (T + P * P))()
+    rc = lib.ring_attn_fwd(_tensor(q), _tensor(k), _tensor(v), B, H, T, d, dt, P, PARTITIONS[partition],
+                           MODES[mode], kpm, kpm_ld, am, am_ld, int(bool(causal)),
+                           0.0 if scale is None else float(scale), int(bool(rope)), float(rope_base),
+                           _ptr(out), _dtype_code(out.dtype), _ptr(lse),
+                           None if maps is None else ctypes.cast(maps, ctypes.c_void_p),
+                           _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("ring_attn_fwd", rc)
+    if return_index_maps:
+        import numpy as np
+        arr = np.ctypeslib.as_array(maps).copy()
+        return out, lse, arr[:T].reshape(P, T // P), arr[T:].reshape(P, P)
+    return out, lse
+
+
+def rope_apply(x, *, base=10000.0, positions=None, out=None, stream=None):
+    """Rotary position embedding of x (B, H, T, d) into a contiguous output."""
+    lib = load()
+    B, H, T, d = x.shape
+    if out is None:
+        out = torch.empty((B, H, T, d), dtype=x.dtype, device=x.device)
+    if positions is not None and (positions.dtype != torch.int32 or not positions.is_cuda):
+        raise ValueError("positions: int32 CUDA tensor")
+    _check("rope_apply", lib.rope_apply(_tensor(x), B, H, T, d, _dtype_code(x.dtype), _ptr(positions),
+                                        float(base), _ptr(out), _stream(stream)))
+    return out
+
+
+def tile_classes(B, Lq, Lk, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None, causal=False,
+                 device="cuda", stream=None):
+    """int8 (B, ceil(Lq/128), ceil(Lk/128)) tile classes computed on the device."""
+    lib = load()
+    out = torch.empty((B, -(-Lq // 128), -(-Lk // 128)), dtype=torch.int8, device=device)
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    _check("ba_tile_classes", lib.ba_tile_classes(B, Lq, Lk, q_off, k_off, kpm, kpm_ld, am, am_ld,
+                                                  int(bool(causal)), _ptr(out), _stream(stream)))
+    return out
+
+
+def index_maps(T, P, partition="contiguous"):
+    """Host, exact: (tok_of (P, T/P) int32, schedule (P, P) int32)."""
+    import numpy as np
+    lib = load()
+    tok = np.zeros(T, dtype=np.int32)
+    sch = np.zeros(P * P, dtype=np.int32)
+    _check("ba_index_maps", lib.ba_index_maps(T, P, PARTITIONS[partition], tok.ctypes.data_as(ctypes.c_void_p),
+                                              sch.ctypes.data_as(ctypes.c_void_p)))
+    return tok.reshape(P, T // P), sch.reshape(P, P)
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise and return BA_OK, or BA_ERR_TIMEOUT when a bounded device wait expired."""
+    return load().ba_sync_status(_stream(stream))
+
+
+def debug_wait_timeout(timeout_ns: int, stream=None):
+    _check("ba_debug_wait_timeout", load().ba_debug_wait_timeout(int(timeout_ns), _stream(stream)))

@@ -1,0 +1,645 @@
+// C-ABI entry points of libblockattn.so (declared in include/blockattn.h):
+// argument checks, geometry set-up, workspace carving, TMA descriptors and
+// kernel dispatch, plus the bandwidth-bound kernels (LSE merge, RoPE, tile
+// classes) and the host-side index maps.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+using namespace ba;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// device error word (one per device, lives as long as the module)
+// ---------------------------------------------------------------------------
+__device__ unsigned g_err_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev < kMaxDevices ? dev : -1;
+}
+
+// Per-device set-up, done once with the device current: the address of the
+// error word and the SM count.
+int device_setup(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_ptr[dev]) return BA_OK;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return BA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BA_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<unsigned *>(p);
+    return BA_OK;
+}
+
+int get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return BA_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return BA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return BA_OK;
+}
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
+
+size_t elem_size(int dtype) { return dtype == BA_F32 ? 4 : 2; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool valid_dtype(int t) { return t == BA_F32 || t == BA_BF16; }
+bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// (B, H, rows, d) bf16 tensor map: 4-D, box 64 columns x 128 rows, 128B swizzle.
+int encode_map(CUtensorMap *m, const void *base, int d, long long rows, int H, int B, long long sT, long long sH,
+               long long sB) {
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)TILE, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BA_OK : BA_ERR_CUDA;
+}
+
+// TMA needs 16-byte aligned bases and byte strides; B or H of 1 may carry any stride.
+bool tma_ok(const ba_tensor &t, int B, int H) {
+    auto al = [](long long s) { return (s * 2) % 16 == 0 && s >= 0; };
+    if (reinterpret_cast<uintptr_t>(t.ptr) % 16) return false;
+    if (!al(t.sT)) return false;
+    if (H > 1 && !al(t.sH)) return false;
+    if (B > 1 && !al(t.sB)) return false;
+    return true;
+}
+
+ba_tensor fix_unit_strides(ba_tensor t, int B, int H, int rows, int d) {
+    // A size-1 axis may have any stride; give it a legal one for TMA.
+    if (H <= 1) t.sH = (long long)rows * t.sT > 0 ? (long long)rows * t.sT : d;
+    if (B <= 1) t.sB = (long long)H * t.sH > 0 ? (long long)H * t.sH : d;
+    return t;
+}
+
+int heads_per_group(int B, int H, long long keys, int d, int dtype) {
+    const double per_head = 2.0 * (double)keys * d * elem_size(dtype);
+    long long G = (long long)(48.0 * 1024 * 1024 / (per_head > 1 ? per_head : 1));
+    if (G < 1) G = 1;
+    if (G > (long long)B * H) G = (long long)B * H;
+    return (int)(G < 1 ? 1 : G);
+}
+
+// ---------------------------------------------------------------------------
+// small kernels
+// ---------------------------------------------------------------------------
+
+// Class of every (b, q tile, k tile) of the walk geometry: one CTA per tile
+// pair, one thread per query row.
+__global__ void tile_class_kernel(const Geom g, int8_t *cls) {
+    const int kg = blockIdx.x, qg = blockIdx.y, b = blockIdx.z;
+    const QTile q = q_tile(g, qg, b, 0);
+    const KTile k = k_tile_by_id(g, kg);
+    const int i = threadIdx.x;
+    int any = 0, all = 1;
+    if (i < q.len) {
+        const long long qp = q.pos0 + i;
+        for (int j = 0; j < k.len; ++j) {
+            const bool vis = !excluded(g, b, qp, k.pos0 + j);
+            any |= vis;
+            all &= vis;
+        }
+    }
+    any = __syncthreads_or(any);
+    all = __syncthreads_and(all);
+    if (i == 0) cls[((long long)b * g.n_qtiles + qg) * g.n_ktiles + kg] =
+        (int8_t)(!any ? BA_TILE_EMPTY : (all ? BA_TILE_FULL : BA_TILE_PARTIAL));
+}
+
+// a <- merge(a, b): one warp per row.
+__global__ void merge_kernel(float *__restrict__ oa, float *__restrict__ la, const float *__restrict__ ob,
+                             const float *__restrict__ lb, long long rows, int d) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const float A = la[r], Bv = lb[r];
+        float wa, wb, L;
+        if (Bv == -INFINITY) {
+            continue;   // nothing to fold in: a unchanged
+        } else if (A == -INFINITY) {
+            wa = 0.f;
+            wb = 1.f;
+            L = Bv;
+        } else {
+            const float M = fmaxf(A, Bv);
+            L = M + logf(expf(A - M) + expf(Bv - M));
+            wa = expf(A - L);
+            wb = expf(Bv - L);
+        }
+        float *pa = oa + r * d;
+        const float *pb = ob + r * d;
+        if ((d & 3) == 0) {
+            float4 *va = reinterpret_cast<float4 *>(pa);
+            const float4 *vb = reinterpret_cast<const float4 *>(pb);
+            for (int c = lane; c < d / 4; c += 32) {
+                const float4 y = vb[c];
+                float4 x = wa != 0.f ? va[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                x.x = wa * x.x + wb * y.x;
+                x.y = wa * x.y + wb * y.y;
+                x.z = wa * x.z + wb * y.z;
+                x.w = wa * x.w + wb * y.w;
+                va[c] = x;
+            }
+        } else {
+            for (int c = lane; c < d; c += 32) pa[c] = (wa != 0.f ? wa * pa[c] : 0.f) + wb * pb[c];
+        }
+        if (lane == 0) la[r] = L;
+    }
+}
+
+struct Thetas {
+    double th[64];
+};
+
+// fp64 -> bf16 with one rounding (ties to even): truncate to fp32, make the
+// result's last bit sticky when inexact (round-to-odd), then round to bf16.
+__device__ __forceinline__ __nv_bfloat16 round_bf16_from_f64(double y) {
+    float f = __double2float_rz(y);
+    if ((double)f != y && isfinite(f)) f = __uint_as_float(__float_as_uint(f) | 1u);
+    return __float2bfloat16_rn(f);
+}
+
+template <typename T>
+__device__ __forceinline__ double ld(const T *p);
+template <>
+__device__ __forceinline__ double ld<float>(const float *p) { return (double)*p; }
+template <>
+__device__ __forceinline__ double ld<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return (double)__bfloat162float(*p);
+}
+__device__ __forceinline__ void st(float *p, double y) { *p = __double2float_rn(y); }
+__device__ __forceinline__ void st(__nv_bfloat16 *p, double y) { *p = round_bf16_from_f64(y); }
+
+// One thread per (position t, pair c); the angle's cos/sin are computed once
+// and applied to that pair in every (b, h).
+template <typename T>
+__global__ void rope_kernel(const T *__restrict__ x, long long sB, long long sH, long long sT, int B, int H, int Tn,
+                            int d, const int32_t *__restrict__ positions, const Thetas th, T *__restrict__ y) {
+    const int half = d / 2;
+    const long long n = (long long)Tn * half;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(e / half), c = (int)(e % half);
+        const double m = positions ? (double)positions[t] : (double)t;
+        double sn, cs;
+        sincos(m * th.th[c], &sn, &cs);
+        for (int b = 0; b < B; ++b) {
+            for (int h = 0; h < H; ++h) {
+                const T *px = x + b * sB + h * sH + t * sT + 2 * c;
+                const double x0 = ld(px), x1 = ld(px + 1);
+                const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
+                const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
+                T *py = y + (((long long)b * H + h) * Tn + t) * d + 2 * c;
+                st(py, y0);
+                st(py + 1, y1);
+            }
+        }
+    }
+}
+
+// Waits on an mbarrier nothing completes; the bounded wait gives up and
+// records a timeout.
+__global__ void wait_timeout_kernel(unsigned *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t barrier_word;
+    __shared__ int abort_flag;
+    const uint32_t bar = smem_u32(&barrier_word);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(bar, 0, &abort_flag, err, limit_ns);
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// shared host helpers
+// ---------------------------------------------------------------------------
+
+// Stream-ordered scratch: caller's buffer, or cudaMallocAsync'd and freed on
+// the stream when the call is done.
+struct Scratch {
+    void *ptr = nullptr;
+    bool owned = false;
+    cudaStream_t s = nullptr;
+    int acquire(void *ws, size_t ws_bytes, size_t need, cudaStream_t stream) {
+        s = stream;
+        if (need == 0) return BA_OK;
+        if (ws) {
+            if (ws_bytes < need) return BA_ERR_WORKSPACE;
+            ptr = ws;
+            return BA_OK;
+        }
+        if (cudaMallocAsync(&ptr, need, stream) != cudaSuccess) return BA_ERR_CUDA;
+        owned = true;
+        return BA_OK;
+    }
+    ~Scratch() {
+        if (owned && ptr) cudaFreeAsync(ptr, s);
+    }
+};
+
+int run_tile_classes(const Geom &g, int8_t *cls, cudaStream_t s) {
+    if (g.n_qtiles == 0 || g.n_ktiles == 0 || g.B == 0) return BA_OK;
+    if (g.n_qtiles > 65535 || g.B > 65535) return BA_ERR_SHAPE;
+    dim3 grid(g.n_ktiles, g.n_qtiles, g.B);
+    tile_class_kernel<<<grid, TILE, 0, s>>>(g, cls);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+int launch_rope(const ba_tensor &x, int B, int H, int T, int d, int dtype, const int32_t *pos, float base, void *y,
+                cudaStream_t s) {
+    Thetas th;
+    for (int c = 0; c < d / 2; ++c) th.th[c] = std::pow((double)base, -(double)(2 * c) / (double)d);
+    const long long n = (long long)T * (d / 2);
+    if (n == 0 || B == 0 || H == 0) return BA_OK;
+    const int threads = 256;
+    long long blocks = (n + threads - 1) / threads;
+    if (blocks > 1 << 20) blocks = 1 << 20;
+    if (dtype == BA_BF16)
+        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(x.ptr), x.sB, x.sH, x.sT, B, H, T, d, pos, th,
+            static_cast<__nv_bfloat16 *>(y));
+    else
+        rope_kernel<float><<<(unsigned)blocks, threads, 0, s>>>(static_cast<const float *>(x.ptr), x.sB, x.sH,
+                                                                 x.sT, B, H, T, d, pos, th, static_cast<float *>(y));
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+// Launch the attention kernel that matches dtype and d.
+int run_attention(AttnArgs &a, int dev, int nrows_q, int nrows_k, cudaStream_t s) {
+    if (!tc_supported(a.dtype, a.g.d) || nrows_k == 0 || nrows_q == 0) return launch_attn_simt(a, s);
+    int rc = get_encoder();
+    if (rc) return rc;
+    TmaMaps m;
+    const int B = a.g.B, H = a.g.H, d = a.g.d;
+    if ((rc = encode_map(&m.q, a.q, d, nrows_q, H, B, a.qsT, a.qsH, a.qsB))) return rc;
+    if ((rc = encode_map(&m.k, a.k, d, nrows_k, H, B, a.ksT, a.ksH, a.ksB))) return rc;
+    if ((rc = encode_map(&m.v, a.v, d, nrows_k, H, B, a.vsT, a.vsH, a.vsB))) return rc;
+    return launch_attn_tc(a, m, g_num_sms[dev], s);
+}
+
+int check_tensor(const ba_tensor &t) { return t.ptr ? BA_OK : BA_ERR_ARG; }
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+extern "C" {
+
+const char *ba_strerror(int code) {
+    switch (code) {
+        case BA_OK: return "ok";
+        case BA_ERR_ARG: return "invalid argument";
+        case BA_ERR_SHAPE: return "unsupported shape";
+        case BA_ERR_CUDA: return "CUDA error";
+        case BA_ERR_TIMEOUT: return "device wait timed out";
+        case BA_ERR_UNSUPPORTED: return "unsupported combination";
+        case BA_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown error";
+    }
+}
+
+int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule) {
+    if (T < 0 || P < 1) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
+    if (T % NC) return BA_ERR_SHAPE;
+    const int CL = T / NC, per = T / P;
+    if (tok_of) {
+        for (int r = 0; r < P; ++r) {
+            // chunks of rank r in its local order
+            const int c0 = r, c1 = 2 * P - 1 - r;
+            for (int t = 0; t < per; ++t) {
+                int tok;
+                if (partition == BA_PART_CONTIGUOUS)
+                    tok = r * CL + t;
+                else
+                    tok = t < CL ? c0 * CL + t : c1 * CL + (t - CL);
+                tok_of[(long long)r * per + t] = tok;
+            }
+        }
+    }
+    if (schedule) {
+        for (int r = 0; r < P; ++r)
+            for (int s = 0; s < P; ++s) schedule[r * P + s] = ((r - s) % P + P) % P;
+    }
+    return BA_OK;
+}
+
+int ba_sync_status(ba_stream_t stream) {
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return BA_ERR_CUDA;
+    unsigned w = 0;
+    if (cudaMemcpy(&w, g_err_ptr[dev], sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return BA_ERR_CUDA;
+    if (w) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(g_err_ptr[dev], &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return BA_ERR_CUDA;
+        return BA_ERR_TIMEOUT;
+    }
+    return BA_OK;
+}
+
+int ba_debug_wait_timeout(int64_t timeout_ns, ba_stream_t stream) {
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    if (timeout_ns < 0) return BA_ERR_ARG;
+    if (timeout_ns > 2000000000LL) timeout_ns = 2000000000LL;
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(g_err_ptr[dev], (unsigned long long)timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_b, int64_t rows, int d,
+               ba_stream_t stream) {
+    if (!out_a || !lse_a || !out_b || !lse_b || rows < 0 || d < 1) return BA_ERR_ARG;
+    if (rows == 0) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    long long blocks = (rows + 7) / 8;
+    const long long cap = (long long)g_num_sms[dev] * 16;
+    if (blocks > cap) blocks = cap;
+    merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out_a, lse_a, out_b, lse_b, rows, d);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+int rope_apply(ba_tensor x, int B, int H, int T, int d, int dtype, const int32_t *positions, float base, void *y,
+               ba_stream_t stream) {
+    if (!x.ptr || !y || B < 0 || H < 0 || T < 0 || d < 2 || (d & 1) || d > 128 || !valid_dtype(dtype) ||
+        !(base > 0.f))
+        return BA_ERR_ARG;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    return launch_rope(x, B, H, T, d, dtype, positions, base, y, stream);
+}
+
+int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off, const uint8_t *key_padding_mask,
+                    int64_t kpm_ld, const uint8_t *attn_mask, int64_t am_ld, int causal, int8_t *classes,
+                    ba_stream_t stream) {
+    if (B < 0 || Lq < 0 || Lk < 0 || q_off < 0 || k_off < 0 || !classes) return BA_ERR_ARG;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    Geom g;
+    std::memset(&g, 0, sizeof g);
+    g.B = B;
+    g.H = 1;
+    g.Lq = Lq;
+    g.Lk = Lk;
+    g.q_off = q_off;
+    g.k_off = k_off;
+    g.nqt_pc = g.n_qtiles = ceil_div(Lq, TILE);
+    g.nkt_pc = g.n_ktiles = ceil_div(Lk, TILE);
+    g.causal = causal != 0;
+    g.kpm = key_padding_mask;
+    g.kpm_ld = kpm_ld;
+    g.am = attn_mask;
+    g.am_ld = am_ld;
+    return run_tile_classes(g, classes, stream);
+}
+
+size_t attn_block_fwd_workspace_size(int B, int Lq, int Lk, int has_masks) {
+    if (!has_masks) return 0;
+    return align256((size_t)B * ceil_div(Lq, TILE) * ceil_div(Lk, TILE));
+}
+
+int attn_block_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,
+                   int64_t q_off, int64_t k_off, const uint8_t *key_padding_mask, int64_t kpm_ld,
+                   const uint8_t *attn_mask, int64_t am_ld, int causal, float scale, void *out, int out_dtype,
+                   float *lse, int accumulate, void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_off < 0 || k_off < 0 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    const bool rows_exist = (long long)B * H * Lq > 0;
+    if (rows_exist && (check_tensor(q) || !out || !lse)) return BA_ERR_ARG;
+    if (rows_exist && Lk > 0 && (check_tensor(k) || check_tensor(v))) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
+    if (accumulate && out_dtype != BA_F32) return BA_ERR_ARG;
+    if ((key_padding_mask && kpm_ld < k_off + Lk) || (attn_mask && am_ld < k_off + Lk)) return BA_ERR_ARG;
+    if (B == 0 || H == 0 || Lq == 0) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    const bool tc = tc_supported(dtype, d) && Lk > 0;
+    q = fix_unit_strides(q, B, H, Lq, d);
+    k = fix_unit_strides(k, B, H, Lk, d);
+    v = fix_unit_strides(v, B, H, Lk, d);
+    if (tc && (!tma_ok(q, B, H) || !tma_ok(k, B, H) || !tma_ok(v, B, H))) return BA_ERR_ARG;
+
+    AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    Geom &g = a.g;
+    g.B = B;
+    g.H = H;
+    g.d = d;
+    g.Lq = Lq;
+    g.Lk = Lk;
+    g.q_off = q_off;
+    g.k_off = k_off;
+    g.nqt_pc = g.n_qtiles = ceil_div(Lq, TILE);
+    g.nkt_pc = g.n_ktiles = ceil_div(Lk, TILE);
+    g.heads_per_group = heads_per_group(B, H, Lk, d, dtype);
+    g.n_items = g.n_qtiles * B * H;
+    g.causal = causal != 0;
+    g.kpm = key_padding_mask;
+    g.kpm_ld = kpm_ld;
+    g.am = attn_mask;
+    g.am_ld = am_ld;
+
+    const bool masks = key_padding_mask || attn_mask;
+    Scratch ws;
+    if ((rc = ws.acquire(workspace, workspace_bytes, attn_block_fwd_workspace_size(B, Lq, Lk, masks), stream)))
+        return rc;
+    if (masks) {
+        g.cls = static_cast<const int8_t *>(ws.ptr);
+        if ((rc = run_tile_classes(g, static_cast<int8_t *>(ws.ptr), stream))) return rc;
+    }
+    a.q = q.ptr;
+    a.k = k.ptr;
+    a.v = v.ptr;
+    a.qsB = q.sB; a.qsH = q.sH; a.qsT = q.sT;
+    a.ksB = k.sB; a.ksH = k.sH; a.ksT = k.sT;
+    a.vsB = v.sB; a.vsH = v.sH; a.vsT = v.sT;
+    a.dtype = dtype;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.scale_log2 = sc * LOG2E;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse;
+    a.rows = Lq;
+    a.acc_o = accumulate ? static_cast<const float *>(out) : nullptr;
+    a.acc_lse = accumulate ? lse : nullptr;
+    a.err = g_err_ptr[dev];
+    a.wait_limit_ns = kWaitLimitNs;
+    return run_attention(a, dev, Lq, Lk, stream);
+}
+
+size_t ring_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype, int P, int partition, int mode,
+                                    int has_masks, int rope, int out_dtype) {
+    if (P < 1 || T < 0) return 0;
+    const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
+    if (NC == 0 || T % NC) return 0;
+    const int CL = T / NC;
+    const size_t nt = (size_t)NC * ceil_div(CL, TILE);
+    size_t bytes = 0;
+    if (has_masks) bytes += align256((size_t)B * nt * nt);
+    const size_t tensor = (size_t)B * H * T * d;
+    if (rope) bytes += 2 * align256(tensor * elem_size(dtype));
+    if (mode == BA_MODE_STEPWISE && P > 1 && out_dtype != BA_F32) bytes += align256(tensor * 4);
+    return bytes;
+}
+
+int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, int d, int dtype, int P, int partition,
+                  int mode, const uint8_t *key_padding_mask, int64_t kpm_ld, const uint8_t *attn_mask, int64_t am_ld,
+                  int causal, float scale, int rope, float rope_base, void *out, int out_dtype, float *lse,
+                  int32_t *index_maps_out, void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || P < 1 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    if ((long long)B * H * T > 0 && (check_tensor(q) || check_tensor(k) || check_tensor(v) || !out || !lse))
+        return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    if (mode != BA_MODE_STEPWISE && mode != BA_MODE_FUSED) return BA_ERR_ARG;
+    if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    if (rope && ((d & 1) || !(rope_base > 0.f))) return BA_ERR_ARG;
+    if ((key_padding_mask && kpm_ld < T) || (attn_mask && am_ld < T)) return BA_ERR_ARG;
+    const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
+    if (T % NC) return BA_ERR_SHAPE;
+    if (index_maps_out) {
+        int rc = ba_index_maps(T, P, partition, index_maps_out, index_maps_out + T);
+        if (rc) return rc;
+    }
+    if (B == 0 || H == 0 || T == 0) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    const bool tc = tc_supported(dtype, d);
+    q = fix_unit_strides(q, B, H, T, d);
+    k = fix_unit_strides(k, B, H, T, d);
+    v = fix_unit_strides(v, B, H, T, d);
+    if (tc && !tma_ok(v, B, H)) return BA_ERR_ARG;
+    if (tc && !rope && (!tma_ok(q, B, H) || !tma_ok(k, B, H))) return BA_ERR_ARG;
+
+    const bool masks = key_padding_mask || attn_mask;
+    Scratch ws;
+    const size_t need = ring_attn_fwd_workspace_size(B, H, T, d, dtype, P, partition, mode, masks, rope, out_dtype);
+    if ((rc = ws.acquire(workspace, workspace_bytes, need, stream))) return rc;
+    uint8_t *wp = static_cast<uint8_t *>(ws.ptr);
+
+    AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    Geom &g = a.g;
+    g.B = B;
+    g.H = H;
+    g.d = d;
+    g.ring = 1;
+    g.T = T;
+    g.P = P;
+    g.zigzag = partition == BA_PART_ZIGZAG;
+    g.NC = NC;
+    g.CL = T / NC;
+    g.nqt_pc = g.nkt_pc = ceil_div(g.CL, TILE);
+    g.n_qtiles = g.n_ktiles = NC * g.nqt_pc;
+    g.heads_per_group = heads_per_group(B, H, T, d, dtype);
+    g.n_items = g.n_qtiles * B * H;
+    g.causal = causal != 0;
+    g.kpm = key_padding_mask;
+    g.kpm_ld = kpm_ld;
+    g.am = attn_mask;
+    g.am_ld = am_ld;
+    g.s_begin = 0;
+    g.s_end = P;
+
+    if (masks) {
+        g.cls = reinterpret_cast<const int8_t *>(wp);
+        if ((rc = run_tile_classes(g, reinterpret_cast<int8_t *>(wp), stream))) return rc;
+        wp += align256((size_t)B * g.n_qtiles * g.n_ktiles);
+    }
+    const size_t tensor = (size_t)B * H * T * d;
+    if (rope) {
+        void *qr = wp;
+        wp += align256(tensor * elem_size(dtype));
+        void *kr = wp;
+        wp += align256(tensor * elem_size(dtype));
+        if ((rc = launch_rope(q, B, H, T, d, dtype, nullptr, rope_base, qr, stream))) return rc;
+        if ((rc = launch_rope(k, B, H, T, d, dtype, nullptr, rope_base, kr, stream))) return rc;
+        const long long sT = d, sH = (long long)T * d, sB = (long long)H * T * d;
+        q = ba_tensor{qr, sB, sH, sT};
+        k = ba_tensor{kr, sB, sH, sT};
+    }
+    a.q = q.ptr;
+    a.k = k.ptr;
+    a.v = v.ptr;
+    a.qsB = q.sB; a.qsH = q.sH; a.qsT = q.sT;
+    a.ksB = k.sB; a.ksH = k.sH; a.ksT = k.sT;
+    a.vsB = v.sB; a.vsH = v.sH; a.vsT = v.sT;
+    a.dtype = dtype;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.scale_log2 = sc * LOG2E;
+    a.lse = lse;
+    a.rows = T;
+    a.err = g_err_ptr[dev];
+    a.wait_limit_ns = kWaitLimitNs;
+
+    if (mode == BA_MODE_FUSED || P == 1) {
+        a.out = out;
+        a.out_dtype = out_dtype;
+        return run_attention(a, dev, T, T, stream);
+    }
+    // Step-wise: one launch per ring step, each folding the step's block into
+    // the fp32 (out, lse) accumulator; the last step writes the final dtype.
+    float *acc = out_dtype == BA_F32 ? static_cast<float *>(out) : reinterpret_cast<float *>(wp);
+    for (int s = 0; s < P; ++s) {
+        g.s_begin = s;
+        g.s_end = s + 1;
+        a.acc_o = s > 0 ? acc : nullptr;
+        a.acc_lse = s > 0 ? lse : nullptr;
+        const bool last = s == P - 1;
+        a.out = last ? out : acc;
+        a.out_dtype = last ? out_dtype : BA_F32;
+        if ((rc = run_attention(a, dev, T, T, stream))) return rc;
+    }
+    return BA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,545 @@
+// Tensor-core attention kernel for sm_103a (bf16 Q/K/V, head dim 64 or 128).
+//
+// Persistent CTAs (one per SM) take work items = (query tile of 128 rows,
+// batch item, head).  For each item the query tile stays resident in shared
+// memory while the key tiles of its walk arrive in ring order; every tile is
+// folded into a running (row max, denominator, weighted sum) that is rescaled
+// to the new maximum, never added or averaged (brunomaga "Improving numerical
+// stability"; llm-systems "Circulate K/V blocks with Ring").
+//
+// Roles (256 threads):
+//   warp 0      TMA producer: Q tile, then K and V tiles into two stage rings
+//               (128B-swizzled boxes of 64 columns x 128 rows).
+//   warp 1      owns TMEM (512 columns) and issues tcgen05.mma from one thread:
+//               S = Q K^T (A, B from shared memory, fp32 accumulate in TMEM),
+//               O += P V (A = P from TMEM, B = V from shared memory).
+//   warps 4..7  softmax: thread t owns query row t (TMEM lane t).  Reads S,
+//               applies scale and exclusions, updates (m, l), writes P (bf16)
+//               to TMEM, rescales O when the row maximum grows by more than
+//               2^8, and at the end normalises O and stores out / lse.
+//   warps 2..3  idle.
+// S is double buffered so the MMA for tile j+1 overlaps the softmax of tile j;
+// P is double buffered so the softmax of tile j+1 overlaps the PV of tile j.
+//
+// TMEM columns: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,384+D).
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// BA_ERR_TIMEOUT in the error word, drains its outstanding copies and MMAs
+// (with bounded waits), frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+
+namespace ba {
+namespace {
+
+template <int D>
+struct Cfg {
+    static constexpr int NBOX = D / 64;            // 64-column boxes per tile
+    static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
+    static constexpr int KS = D == 128 ? 3 : 4;    // K stages
+    static constexpr int VS = D == 128 ? 3 : 4;    // V stages
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
+    enum {
+        B_QFULL = 0,
+        B_QEMPTY,
+        B_KFULL,
+        B_KEMPTY = B_KFULL + KS,
+        B_VFULL = B_KEMPTY + KS,
+        B_VEMPTY = B_VFULL + VS,
+        B_SFULL = B_VEMPTY + VS,
+        B_SEMPTY = B_SFULL + 2,
+        B_PFULL = B_SEMPTY + 2,
+        B_PVDONE = B_PFULL + 2,
+        B_OFULL = B_PVDONE + 2,
+        B_OEMPTY,
+        B_DRAIN,
+        NBAR
+    };
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort flag
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
+    static constexpr uint32_t S_COL = 0;
+    static constexpr uint32_t P_COL = 256;
+    static constexpr uint32_t O_COL = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    // Instruction descriptors (kind::f16): D fp32 (bits 4-5 = 1), A and B
+    // bf16 (bits 7-9, 10-12 = 1), B major bit 16 (0 = K-major, 1 = MN-major),
+    // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+    static constexpr uint32_t IDESC_QK =
+        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TILE >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+    static constexpr uint32_t IDESC_PV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                         ((uint32_t)(D >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+};
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 version field.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive 32-bit TMEM columns of this warp's 32 lanes, one lane per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait by every lane of a warp, with a warp-uniform verdict so that
+// the warp reaches the following .sync.aligned TMEM instructions converged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort, unsigned *err,
+                                          uint64_t lim) {
+    const bool ok = mbar_wait(bar, parity, abort, err, lim);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);   // .x (low half) = lo
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// ----------------------------------------------------------------------------
+// Kernel
+// ----------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_base);
+    const uint32_t sQ = base + C::Q_OFF, sK = base + C::K_OFF, sV = base + C::V_OFF;
+    const uint32_t bars = base + C::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + C::MISC_OFF + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geom &g = a.g;
+    const uint64_t lim = a.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
+        mbar_init(bar(C::B_QEMPTY), 1);
+        for (int i = 0; i < C::KS; ++i) {
+            mbar_init(bar(C::B_KFULL + i), 1);
+            mbar_init(bar(C::B_KEMPTY + i), 1);
+        }
+        for (int i = 0; i < C::VS; ++i) {
+            mbar_init(bar(C::B_VFULL + i), 1);
+            mbar_init(bar(C::B_VEMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_SFULL + i), 1);
+            mbar_init(bar(C::B_SEMPTY + i), 128);
+            mbar_init(bar(C::B_PFULL + i), 128);
+            mbar_init(bar(C::B_PVDONE + i), 1);
+        }
+        mbar_init(bar(C::B_OFULL), 1);
+        mbar_init(bar(C::B_OEMPTY), 128);
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         base + C::MISC_OFF),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const int nwalk = walk_length(g);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t kfill = 0, vfill = 0, qfills = 0, it_local = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
+                const QTile qt = work_item(g, w);
+                if (it_local > 0 && !mbar_wait(bar(C::B_QEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
+                for (int bx = 0; bx < C::NBOX; ++bx)
+                    tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, qt.row0, qt.h, qt.b, bar(C::B_QFULL));
+                ++qfills;
+                for (int it = 0; it < nwalk; ++it) {
+                    const KTile kt = walk_tile(g, qt, it);
+                    if (kt.cls == BA_TILE_EMPTY) continue;
+                    uint32_t st = kfill % C::KS, use = kfill / C::KS;
+                    if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h,
+                                    qt.b, bar(C::B_KFULL + st));
+                    ++kfill;
+                    st = vfill % C::VS;
+                    use = vfill / C::VS;
+                    if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt.row0, qt.h,
+                                    qt.b, bar(C::B_VFULL + st));
+                    ++vfill;
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before the CTA exits.
+                volatile int never = 0;
+                const uint64_t lim2 = 200000000ull;
+                if (qfills > 0) mbar_wait(bar(C::B_QFULL), (qfills - 1) & 1, &never, nullptr, lim2);
+                for (uint32_t i = 0; i < (uint32_t)C::KS && i < kfill; ++i) {
+                    const uint32_t last = kfill - 1 - i;
+                    mbar_wait(bar(C::B_KFULL + last % C::KS), (last / C::KS) & 1, &never, nullptr, lim2);
+                }
+                for (uint32_t i = 0; i < (uint32_t)C::VS && i < vfill; ++i) {
+                    const uint32_t last = vfill - 1 - i;
+                    mbar_wait(bar(C::B_VFULL + last % C::VS), (last / C::VS) & 1, &never, nullptr, lim2);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t kcons = 0, vcons = 0, scnt = 0, pcnt = 0, it_local = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
+                const QTile qt = work_item(g, w);
+                if (!mbar_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool have_prev = false, first_pv = true;
+                auto issue_pv = [&]() -> bool {
+                    const uint32_t vs = vcons % C::VS, pb = pcnt & 1;
+                    if (!mbar_wait(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort, a.err, lim)) return false;
+                    if (!mbar_wait(bar(C::B_PFULL + pb), (pcnt >> 1) & 1, abort, a.err, lim)) return false;
+                    if (first_pv && it_local > 0 &&
+                        !mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t vbase = sV + vs * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TILE / 16; ++kk) {
+                        uint64_t bd = sdesc(vbase + kk * 2048, C::BOX_BYTES, 1024);
+                        mma_ts(tmem + C::O_COL, tmem + C::P_COL + pb * 64 + kk * 8, bd, C::IDESC_PV,
+                               (first_pv && kk == 0) ? 0u : 1u);
+                    }
+                    mma_commit(bar(C::B_VEMPTY + vs));
+                    mma_commit(bar(C::B_PVDONE + pb));
+                    ++vcons;
+                    ++pcnt;
+                    first_pv = false;
+                    return true;
+                };
+                for (int it = 0; it < nwalk && ok; ++it) {
+                    const KTile kt = walk_tile(g, qt, it);
+                    if (kt.cls == BA_TILE_EMPTY) continue;
+                    const uint32_t ks = kcons % C::KS, sb = scnt & 1;
+                    if (!mbar_wait(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    if (scnt >= 2 && !mbar_wait(bar(C::B_SEMPTY + sb), ((scnt >> 1) - 1) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = sK + ks * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                        mma_ss(tmem + C::S_COL + sb * 128, sdesc(sQ + off, 16, 1024), sdesc(kbase + off, 16, 1024),
+                               C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(C::B_SFULL + sb));
+                    mma_commit(bar(C::B_KEMPTY + ks));
+                    ++kcons;
+                    ++scnt;
+                    if (have_prev && !issue_pv()) {
+                        ok = false;
+                        break;
+                    }
+                    have_prev = true;
+                }
+                if (!ok) break;
+                mma_commit(bar(C::B_QEMPTY));
+                if (have_prev && !issue_pv()) {
+                    ok = false;
+                    break;
+                }
+                mma_commit(bar(C::B_OFULL));
+            }
+            if (!ok) {
+                // Wait for the MMAs already issued before TMEM is released.
+                volatile int never = 0;
+                mma_commit(bar(C::B_DRAIN));
+                mbar_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_addr = ((uint32_t)((warp & 3) * 32) << 16);
+        const float sl2 = a.scale_log2;
+        uint32_t scnt = 0, it_local = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
+            const QTile qt = work_item(g, w);
+            const long long qpos = qt.pos0 + row;
+            float m_ref = -INFINITY, l = 0.f;
+            int n = 0;
+            for (int it = 0; it < nwalk; ++it) {
+                const KTile kt = walk_tile(g, qt, it);
+                if (kt.cls == BA_TILE_EMPTY) continue;
+                const uint32_t sb = scnt & 1;
+                if (!warp_wait(bar(C::B_SFULL + sb), (scnt >> 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[TILE];
+#pragma unroll
+                for (int c = 0; c < TILE / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                }
+                tc_fence_before();
+                mbar_arrive(bar(C::B_SEMPTY + sb));
+
+                const bool need_mask = kt.cls == BA_TILE_PARTIAL || kt.len < TILE;
+                const bool row_valid = row < qt.len;   // rows past the tile end are never stored
+                float mx = -INFINITY;
+                if (need_mask) {
+#pragma unroll
+                    for (int j = 0; j < TILE; ++j) {
+                        if (j >= kt.len || (row_valid && excluded(g, qt.b, qpos, kt.pos0 + j))) s[j] = -INFINITY;
+                        mx = fmaxf(mx, s[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < TILE; ++j) mx = fmaxf(mx, s[j]);
+                }
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool resc = m_new > m_ref + 8.0f;   // true when m_ref = -inf and m_new finite
+                float alpha = 1.f;
+                if (resc) {
+                    alpha = fast_exp2(m_ref - m_new);
+                    m_ref = m_new;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                float sum = 0.f;
+                uint32_t pk[TILE / 2];
+#pragma unroll
+                for (int j = 0; j < TILE / 2; ++j) {
+                    const float p0 = fast_exp2(fmaf(s[2 * j], sl2, -m_use));
+                    const float p1 = fast_exp2(fmaf(s[2 * j + 1], sl2, -m_use));
+                    sum += p0 + p1;
+                    pk[j] = pack_bf16(p0, p1);
+                }
+                l = l * alpha + sum;
+
+                const uint32_t pb = scnt & 1;
+                if (scnt >= 2 && !warp_wait(bar(C::B_PVDONE + pb), ((scnt >> 1) - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < TILE / 64; ++c) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = pk[c * 32 + i];
+                    tmem_st32(tmem + lane_addr + C::P_COL + pb * 64 + c * 32, r);
+                }
+                if (__any_sync(0xffffffffu, resc) && n > 0) {
+                    const uint32_t prev = scnt - 1;
+                    if (!warp_wait(bar(C::B_PVDONE + (prev & 1)), (prev >> 1) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_addr + C::O_COL + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tmem + lane_addr + C::O_COL + c * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PFULL + pb));
+                ++scnt;
+                ++n;
+            }
+            if (!ok) break;
+            // epilogue
+            if (!warp_wait(bar(C::B_OFULL), it_local & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool valid = row < qt.len;
+            const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + qt.row0 + row;
+            const float acc_l = (a.acc_lse != nullptr && valid) ? a.acc_lse[row_flat] : -INFINITY;
+            const RowFinal f = row_final(m_ref, n > 0 ? l : 0.f, acc_l);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                float o[32];
+                if (n > 0) {
+                    tmem_ld32(tmem + lane_addr + C::O_COL + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                }
+                if (valid) store_row_chunk(a, row_flat, c * 32, o, 32, f);
+            }
+            if (valid) a.lse[row_flat] = f.lse;
+            tc_fence_before();
+            mbar_arrive(bar(C::B_OEMPTY));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int D>
+int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
+    using C = Cfg<D>;
+    static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return BA_ERR_CUDA;
+    int grid = a.g.n_items < num_sms ? a.g.n_items : num_sms;
+    attn_tc_kernel<D><<<grid, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int d) { return dtype == BA_BF16 && (d == 64 || d == 128); }
+
+size_t tc_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<64>::SMEM_BYTES; }
+
+int launch_attn_tc(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
+    if (a.g.n_items == 0) return BA_OK;
+    if (a.g.d == 128) return launch_d<128>(a, m, num_sms, s);
+    if (a.g.d == 64) return launch_d<64>(a, m, num_sms, s);
+    return BA_ERR_SHAPE;
+}
+
+}  // namespace ba

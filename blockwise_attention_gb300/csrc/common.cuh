@@ -1,0 +1,243 @@
+// Shared device-side pieces of libblockattn: the work geometry (which query
+// tiles exist, which key tiles each of them visits and in what order), the
+// tile classes of the combined exclusion mask, and bounded mbarrier waits.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/blockattn.h"
+
+namespace ba {
+
+constexpr int TILE = 128;               // query rows and keys per tile
+constexpr unsigned ERR_TIMEOUT_BIT = 1u;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// Geometry
+// ---------------------------------------------------------------------------
+//
+// Block mode (attn_block_fwd): query rows [0, Lq) of the q tensor are global
+// positions q_off + i; keys [0, Lk) of k/v are global positions k_off + j.
+// Tiles are cut every 128 rows from the block origin.
+//
+// Ring mode (ring_attn_fwd): q, k, v are (B, H, T, d) in global order.  T is
+// cut into NC equal chunks of CL tokens (NC = P contiguous, 2P zigzag); rank r
+// owns chunk r (contiguous) or chunks r and 2P-1-r (zigzag, local order as
+// listed).  Tiles are cut every 128 tokens from each chunk start, so a chunk
+// whose length is not a multiple of 128 ends in a ragged tile.  A query tile
+// of rank r visits, for ring steps s in [s_begin, s_end), the key tiles of the
+// chunks of rank (r - s) mod P in that rank's local order.
+struct Geom {
+    int B, H, d;
+    int ring;
+    // block mode
+    int Lq, Lk;
+    long long q_off, k_off;
+    // ring mode
+    int T, P, zigzag, CL, NC, s_begin, s_end;
+    // derived
+    int nqt_pc, nkt_pc;      // tiles per q chunk / per k chunk
+    int n_qtiles, n_ktiles;  // per (b, h)
+    int heads_per_group;     // (b, h) pairs interleaved per group of work items
+    int n_items;             // n_qtiles * B * H
+    int causal;
+    const uint8_t *kpm;
+    long long kpm_ld;
+    const uint8_t *am;
+    long long am_ld;
+    const int8_t *cls;       // (B, n_qtiles, n_ktiles) classes, or nullptr (causal only)
+};
+
+struct QTile {
+    int g;              // q tile id within (b, h): 0 .. n_qtiles-1
+    int row0, len;      // first row in the q tensor, valid rows (1..128)
+    long long pos0;     // global position of the first row
+    int rank;           // owning rank (ring mode)
+    int b, h;
+};
+
+struct KTile {
+    int idx;            // key tile id within (b, h): 0 .. n_ktiles-1
+    int row0, len;      // first row in the k/v tensors, valid keys (1..128)
+    long long pos0;     // global position of the first key
+    int cls;            // BA_TILE_*
+};
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Owner rank of chunk c.
+__host__ __device__ inline int chunk_owner(const Geom &g, int c) {
+    if (!g.zigzag) return c;
+    return c < g.P ? c : 2 * g.P - 1 - c;
+}
+
+// Query tile with id qg (0 .. n_qtiles-1) of head (b, h).
+__host__ __device__ inline QTile q_tile(const Geom &g, int qg, int b, int h) {
+    QTile t;
+    t.g = qg;
+    t.b = b;
+    t.h = h;
+    if (g.ring) {
+        int c = qg / g.nqt_pc, i = qg % g.nqt_pc;
+        t.row0 = c * g.CL + i * TILE;
+        int end = (c + 1) * g.CL;
+        t.len = (t.row0 + TILE < end ? t.row0 + TILE : end) - t.row0;
+        t.pos0 = t.row0;
+        t.rank = chunk_owner(g, c);
+    } else {
+        t.row0 = qg * TILE;
+        t.len = (t.row0 + TILE < g.Lq ? t.row0 + TILE : g.Lq) - t.row0;
+        t.pos0 = g.q_off + t.row0;
+        t.rank = 0;
+    }
+    return t;
+}
+
+// Key tile with id kg (0 .. n_ktiles-1), geometry only (class not set).
+__host__ __device__ inline KTile k_tile_by_id(const Geom &g, int kg) {
+    KTile t;
+    t.idx = kg;
+    t.cls = BA_TILE_PARTIAL;
+    if (g.ring) {
+        int c = kg / g.nkt_pc, i = kg % g.nkt_pc;
+        t.row0 = c * g.CL + i * TILE;
+        int end = (c + 1) * g.CL;
+        t.len = (t.row0 + TILE < end ? t.row0 + TILE : end) - t.row0;
+        t.pos0 = t.row0;
+    } else {
+        t.row0 = kg * TILE;
+        t.len = (t.row0 + TILE < g.Lk ? t.row0 + TILE : g.Lk) - t.row0;
+        t.pos0 = g.k_off + t.row0;
+    }
+    return t;
+}
+
+// Number of positions in the key-tile walk of one query tile (EMPTY tiles
+// included; they are skipped by the caller).
+__host__ __device__ inline int walk_length(const Geom &g) {
+    if (!g.ring) return g.n_ktiles;
+    return (g.s_end - g.s_begin) * (g.zigzag ? 2 : 1) * g.nkt_pc;
+}
+
+// Causal class of (q tile, k tile) from positions alone.
+__host__ __device__ inline int causal_class(const QTile &q, const KTile &k) {
+    long long q_last = q.pos0 + q.len - 1;
+    long long k_last = k.pos0 + k.len - 1;
+    if (k.pos0 > q_last) return BA_TILE_EMPTY;
+    if (k_last <= q.pos0) return BA_TILE_FULL;
+    return BA_TILE_PARTIAL;
+}
+
+// it-th key tile of the walk of query tile q, with its class.
+__device__ inline KTile walk_tile(const Geom &g, const QTile &q, int it) {
+    int kg;
+    if (g.ring) {
+        int per_rank = (g.zigzag ? 2 : 1) * g.nkt_pc;
+        int s = g.s_begin + it / per_rank;
+        int rem = it % per_rank;
+        int src = q.rank - s;
+        src = ((src % g.P) + g.P) % g.P;
+        int ci = rem / g.nkt_pc;               // which of src's chunks (local order)
+        int c = ci == 0 ? src : 2 * g.P - 1 - src;
+        kg = c * g.nkt_pc + rem % g.nkt_pc;
+    } else {
+        kg = it;
+    }
+    KTile k = k_tile_by_id(g, kg);
+    if (g.cls) {
+        k.cls = g.cls[((long long)q.b * g.n_qtiles + q.g) * g.n_ktiles + kg];
+    } else {
+        k.cls = g.causal ? causal_class(q, k) : BA_TILE_FULL;
+        // without a class map, masks force per-element predicates
+        if (k.cls == BA_TILE_FULL && (g.kpm || g.am)) k.cls = BA_TILE_PARTIAL;
+    }
+    return k;
+}
+
+// Work item w -> (q tile, b, h).  Items are grouped by heads_per_group (b, h)
+// pairs so that concurrently running CTAs share K/V in L2; within a group the
+// query tiles come heaviest first under causal masking (latest positions).
+__host__ __device__ inline QTile work_item(const Geom &g, int w) {
+    int BH = g.B * g.H;
+    int G = g.heads_per_group;
+    int per_group = G * g.n_qtiles;
+    int grp = w / per_group;
+    int rem = w % per_group;
+    int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
+    int qi = rem / g_heads;
+    int bh = grp * G + rem % g_heads;
+    int qg = g.causal ? g.n_qtiles - 1 - qi : qi;
+    return q_tile(g, qg, bh / g.H, bh % g.H);
+}
+
+// Is key position kp excluded for query position qp of batch item b?
+__device__ inline bool excluded(const Geom &g, int b, long long qp, long long kp) {
+    if (g.causal && kp > qp) return true;
+    if (g.kpm && g.kpm[b * g.kpm_ld + kp]) return true;
+    if (g.am && g.am[qp * g.am_ld + kp]) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier helpers with bounded waits
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity of barrier `bar` has completed.
+// Gives up (returns false) when *abort is set by another role, or after
+// limit_ns nanoseconds, in which case it sets *abort and the error word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned *err, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                if (err) atomicOr(err, ERR_TIMEOUT_BIT);
+                return false;
+            }
+        }
+    }
+}
+
+}  // namespace ba

@@ -1,0 +1,41 @@
+// Host-side interface between the C-ABI entry points (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ba {
+
+// Arguments of one attention launch (block or ring geometry).
+struct AttnArgs {
+    Geom g;
+    const void *q, *k, *v;               // base pointers, dtype `dtype`
+    long long qsB, qsH, qsT;             // element strides (d contiguous)
+    long long ksB, ksH, ksT;
+    long long vsB, vsH, vsT;
+    int dtype;                           // BA_F32 / BA_BF16
+    float scale_log2;                    // softmax scale * log2(e)
+    void *out;                           // (B, H, rows, d) contiguous, out_dtype
+    int out_dtype;
+    float *lse;                          // (B, H, rows) natural-log LSE
+    long long rows;                      // rows of out/lse per (b, h): Lq or T
+    const float *acc_o;                  // nullable fp32 (B, H, rows, d) partial to merge with
+    const float *acc_lse;                // nullable fp32 (B, H, rows)
+    unsigned *err;                       // device error word
+    unsigned long long wait_limit_ns;    // bounded-wait limit
+};
+
+// TMA descriptors of Q, K, V for the tensor-core kernel.
+struct TmaMaps {
+    CUtensorMap q, k, v;
+};
+
+int launch_attn_simt(const AttnArgs &a, cudaStream_t s);
+int launch_attn_tc(const AttnArgs &a, const TmaMaps &maps, int num_sms, cudaStream_t s);
+bool tc_supported(int dtype, int d);
+size_t tc_smem_bytes(int d);
+
+}  // namespace ba

@@ -1,0 +1,205 @@
+/*
+ * blockattn.h -- C ABI of libblockattn.so: blockwise multi-head scaled-dot-
+ * product attention with the Ring-Attention online-softmax (LSE) merge,
+ * hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensor arguments are DEVICE pointers owned by the caller.  The library
+ *    never frees caller memory and never keeps a pointer after a call returns.
+ *  - Q, K, V use the layout (B, H, T, d): `ba_tensor` carries the base pointer
+ *    and element strides of the B, H and T axes; the d axis is contiguous.
+ *    Outputs are contiguous: out (B, H, L, d), lse (B, H, L).
+ *  - Masks are uint8 with 1 = EXCLUDED, indexed at GLOBAL token positions:
+ *      key_padding_mask[b * kpm_ld + key_pos]      (B rows, >= total keys)
+ *      attn_mask[query_pos * am_ld + key_pos]      (>= total queries rows)
+ *    A pair (i, j) takes part iff it is not excluded by causality (j > i,
+ *    when causal != 0), by the key padding of its batch item, or by attn_mask:
+ *    the exclusions are OR-combined ("PyTorch MultiheadAttention", item #2 of
+ *    ai.engineer "Transformers and Attention"; causal = diagonal + lower
+ *    triangle, item #24 "PyTorch scaled_dot_product_attention").
+ *  - lse is the NATURAL-log log-sum-exp of the scaled scores of a row,
+ *    LSE_i = log sum_j exp(s_ij), s_ij = scale * q_i . k_j ("Ring Attention"
+ *    and "Improving numerical stability" on brunomaga "Sequence/context
+ *    parallelism").  A row with no visible key gets out = 0 and lse = -inf.
+ *  - Every call is asynchronous on `stream` and returns BA_OK or a negative
+ *    error code (ba_strerror names it).  Argument errors are detected on the
+ *    host before anything is launched.  A device-side wait that exceeds its
+ *    time limit is reported by ba_sync_status() as BA_ERR_TIMEOUT; kernels
+ *    never trap.
+ *  - Scratch: entry points that need scratch take (workspace, workspace_bytes).
+ *    workspace == NULL makes the library allocate it stream-ordered
+ *    (cudaMallocAsync) and free it on the same stream before returning;
+ *    the *_workspace_size() queries give the bytes a caller should pass.
+ *  - bf16 inputs with d in {64, 128} run on the tcgen05 tensor-core kernel
+ *    (TMA-staged tiles, TMEM accumulators); fp32 inputs, and bf16 with other d
+ *    in {16, 32}, run on a CUDA-core kernel that keeps fp32 arithmetic.
+ */
+#ifndef BLOCKATTN_H
+#define BLOCKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ba_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+    BA_OK = 0,
+    BA_ERR_ARG = -1,         /* bad pointer, size, flag or alignment */
+    BA_ERR_SHAPE = -2,       /* sizes not supported (d, T vs P, ...) */
+    BA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+    BA_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired */
+    BA_ERR_UNSUPPORTED = -5, /* combination not implemented */
+    BA_ERR_WORKSPACE = -6    /* workspace smaller than required */
+};
+
+enum { BA_F32 = 0, BA_BF16 = 1 };
+enum { BA_PART_CONTIGUOUS = 0, BA_PART_ZIGZAG = 1 };
+enum { BA_MODE_STEPWISE = 0, BA_MODE_FUSED = 1 };
+enum { BA_TILE_EMPTY = 0, BA_TILE_FULL = 1, BA_TILE_PARTIAL = 2 };
+
+/* Strided (B, H, T, d) tensor: element (b, h, t, c) is at
+ * ptr + b*sB + h*sH + t*sT + c (in elements of the tensor's dtype). */
+typedef struct {
+    const void *ptr;
+    int64_t sB, sH, sT;
+} ba_tensor;
+
+/*
+ * attn_block_fwd -- one block of attention: the queries of q against the keys
+ * and values of k, v, with per-row LSE.  This is the per-step kernel of the
+ * ring loop (brunomaga "Implementation": each step computes the block output
+ * and the per-row LSE of the local queries against the current K/V block).
+ *
+ *  q: (B, H, Lq, d); local row i is global query position q_off + i.
+ *  k, v: (B, H, Lk, d); local key j is global key position k_off + j.
+ *  dtype: BA_F32 or BA_BF16 (q, k, v share it).  d: 16, 32, 64 or 128.
+ *  key_padding_mask / attn_mask: NULL or as in the conventions above; their
+ *    lds are in elements and must cover the global positions used.
+ *  causal: exclude key positions greater than the query position (global).
+ *  scale: > 0, or <= 0 for 1/sqrt(d).
+ *  out: (B, H, Lq, d) contiguous, out_dtype = BA_F32 or dtype.
+ *  lse: (B, H, Lq) fp32 contiguous.
+ *  accumulate: 0 = overwrite (out, lse); 1 = (out, lse) already hold a partial
+ *    attention of the same rows over other keys (fp32 out required; out = 0,
+ *    lse = -inf means "nothing yet") and the block is merged into it with the
+ *    LSE rule: L = log(e^La + e^Lb), O = e^(La-L) Oa + e^(Lb-L) Ob.
+ *  workspace: see conventions; attn_block_fwd_workspace_size() bytes.
+ * Errors: BA_ERR_ARG (NULL q/k/v/out/lse, negative sizes, accumulate with a
+ * non-fp32 out, misaligned TMA strides), BA_ERR_SHAPE (unsupported d).
+ */
+size_t attn_block_fwd_workspace_size(int B, int Lq, int Lk, int has_masks);
+int attn_block_fwd(ba_tensor q, ba_tensor k, ba_tensor v,
+                   int B, int H, int Lq, int Lk, int d, int dtype,
+                   int64_t q_off, int64_t k_off,
+                   const uint8_t *key_padding_mask, int64_t kpm_ld,
+                   const uint8_t *attn_mask, int64_t am_ld,
+                   int causal, float scale,
+                   void *out, int out_dtype, float *lse, int accumulate,
+                   void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
+ * attn_merge -- a <- merge(a, b) for two partial attentions of the same rows
+ * over disjoint key sets: with M = max(La, Lb), L = M + log(e^(La-M) + e^(Lb-M))
+ * and O = e^(La-L) Oa + e^(Lb-L) Ob; a side with lse = -inf contributes nothing.
+ * This is accumulate_out_and_lse of brunomaga "Implementation"; the outputs of
+ * blocks are never added or averaged (llm-systems "CP: Split Long Contexts
+ * Across GPUs", "Circulate K/V blocks with Ring").
+ *  out_a (rows, d), lse_a (rows): fp32, updated in place.
+ *  out_b (rows, d), lse_b (rows): fp32, read only.  d >= 1.
+ */
+int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_b,
+               int64_t rows, int d, ba_stream_t stream);
+
+/*
+ * ring_attn_fwd -- Ring Attention over P context-parallel ranks emulated on
+ * one GPU (llm-systems "Circulate K/V blocks with Ring"; brunomaga
+ * "Distributed algorithm").  The T tokens are split into P ranks
+ * (partition = BA_PART_CONTIGUOUS: P equal time blocks; BA_PART_ZIGZAG: 2P
+ * equal chunks, rank r owning chunks r and 2P-1-r, llm-systems "Balance the
+ * workload in causal attention").  Every rank keeps its queries resident; at
+ * ring step s = 0..P-1 it folds in the K/V block of rank (r - s) mod P (local
+ * block first, then the previous rank's, ...).  Positions and masks stay the
+ * global ones.  There is no inter-GPU traffic: each rank's "received" block is
+ * the partition already resident in this GPU's memory.
+ *
+ *  q, k, v: (B, H, T, d), dtype as for attn_block_fwd.
+ *  mode: BA_MODE_FUSED = one persistent launch, each query tile walks the
+ *    whole ring in-kernel with the running (max, denominator, weighted sum);
+ *    BA_MODE_STEPWISE = one launch per ring step, each merging its block
+ *    into an fp32 (out, lse) accumulator (the page's loop, step by step).
+ *  rope != 0: Q and K are first rotated (see rope_apply, positions 0..T-1,
+ *    base rope_base) into workspace copies; the caller's q, k are unchanged.
+ *  out: (B, H, T, d) in global token order, out_dtype BA_F32 or dtype.
+ *  lse: (B, H, T) fp32.
+ *  index_maps_out: NULL, or host int32[T + P*P] receiving the partition
+ *    (rank-major token ids, P x T/P) followed by the schedule src[r][s].
+ * Errors: BA_ERR_SHAPE when T is not divisible by P (contiguous) or 2P
+ * (zigzag), or d is unsupported; BA_ERR_ARG as for attn_block_fwd.
+ */
+size_t ring_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype, int P,
+                                    int partition, int mode, int has_masks, int rope,
+                                    int out_dtype);
+int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v,
+                  int B, int H, int T, int d, int dtype,
+                  int P, int partition, int mode,
+                  const uint8_t *key_padding_mask, int64_t kpm_ld,
+                  const uint8_t *attn_mask, int64_t am_ld,
+                  int causal, float scale, int rope, float rope_base,
+                  void *out, int out_dtype, float *lse, int32_t *index_maps_out,
+                  void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
+ * rope_apply -- rotary position embedding ("RoFormer", item #4 of ai.engineer
+ * "Transformers and Attention"): split each d-vector into coordinate pairs
+ * (2c, 2c+1) and rotate pair c by the angle m * base^(-2c/d), m the token
+ * position: (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).  The rotation is
+ * evaluated in fp64 and rounded once (ties to even) to the tensor dtype.
+ *  x: (B, H, T, d) strided input; y: (B, H, T, d) contiguous output of the
+ *  same dtype (may not alias x).  positions: NULL (position of row t is t)
+ *  or device int32[T].  d must be even (else BA_ERR_ARG).
+ */
+int rope_apply(ba_tensor x, int B, int H, int T, int d, int dtype,
+               const int32_t *positions, float base, void *y, ba_stream_t stream);
+
+/*
+ * ba_tile_classes -- class of each 128 x 128 tile of the combined exclusion
+ * mask for the block rows [q_off, q_off+Lq) x keys [k_off, k_off+Lk), tiles
+ * counted from the block origin: BA_TILE_EMPTY (no visible pair), FULL (all
+ * pairs visible) or PARTIAL.  classes: device int8 (B, ceil(Lq/128),
+ * ceil(Lk/128)).  The attention kernels skip EMPTY tiles and apply per-element
+ * predicates on PARTIAL ones.
+ */
+int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off,
+                    const uint8_t *key_padding_mask, int64_t kpm_ld,
+                    const uint8_t *attn_mask, int64_t am_ld, int causal,
+                    int8_t *classes, ba_stream_t stream);
+
+/*
+ * ba_index_maps -- host, exact integers: the emulated ranks' token ownership
+ * tok_of[r * (T/P) + t] (rank r's t-th local token, in its local order) and
+ * the ring schedule schedule[r * P + s] = (r - s) mod P.  Same partitions and
+ * order as ring_attn_fwd.  Returns BA_ERR_SHAPE for indivisible T.
+ */
+int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule);
+
+/* Synchronise `stream` and report whether any kernel launched by this library
+ * on the current device since the previous call gave up a bounded device wait
+ * (BA_ERR_TIMEOUT), or a CUDA error occurred (BA_ERR_CUDA).  Clears the flag. */
+int ba_sync_status(ba_stream_t stream);
+
+/* Test hook for the bounded-wait path: launches one CTA that waits on an
+ * mbarrier nothing will complete, giving up after `timeout_ns` nanoseconds
+ * (capped at 2e9) and recording BA_ERR_TIMEOUT for ba_sync_status. */
+int ba_debug_wait_timeout(int64_t timeout_ns, ba_stream_t stream);
+
+const char *ba_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLOCKATTN_H */

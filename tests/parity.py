@@ -1,0 +1,70 @@
+"""Helpers for comparing the CUDA path with the oracle (test-side only)."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+
+TOL_OUT = {"bf16": 2e-2, "f32": 1e-4}
+TOL_LSE = 1e-5
+
+
+def to_np(x):
+    return x.detach().float().cpu().numpy() if torch.is_tensor(x) else np.asarray(x)
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, dtype, label=""):
+    """Element-wise comparison; returns a stats dict and asserts the tolerances."""
+    o = to_np(out_gpu).reshape(-1, out_ref.shape[-1]).astype(np.float64)
+    l = to_np(lse_gpu).reshape(-1).astype(np.float64)
+    orf = np.asarray(out_ref, dtype=np.float64).reshape(o.shape)
+    lrf = np.asarray(lse_ref, dtype=np.float64).reshape(l.shape)
+    assert np.isfinite(o).all(), f"{label}: non-finite outputs"
+    fin = np.isfinite(lrf)
+    assert np.array_equal(fin, np.isfinite(l)), f"{label}: -inf LSE rows differ"
+    assert np.all(l[~fin] == -np.inf)
+    err_o = float(np.max(np.abs(o - orf))) if o.size else 0.0
+    err_l = float(np.max(np.abs(l[fin] - lrf[fin]))) if fin.any() else 0.0
+    denom = float(np.linalg.norm(orf)) or 1.0
+    rel_l2 = float(np.linalg.norm(o - orf)) / denom
+    stats = {"label": label, "max_abs_out": err_o, "max_abs_lse": err_l,
+             "log10_rel_l2": math.log10(rel_l2) if rel_l2 > 0 else -math.inf, "rows": int(l.size)}
+    print(stats)
+    assert err_o <= TOL_OUT[dtype], stats
+    assert err_l <= TOL_LSE, stats
+    return stats
+
+
+def sample_rows(B, H, T, heads, per_head, chunk, seed=0):
+    """Flat row ids ((b*H + h)*T + i): for each (b, h) in heads, the first and last
+    row of every chunk plus random rows."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for (b, h) in heads:
+        base = (b * H + h) * T
+        edge = sorted({c for s in range(0, T, chunk) for c in (s, min(T, s + chunk) - 1)})
+        rnd = rng.choice(T, size=max(0, per_head - len(edge)), replace=False)
+        sel = np.unique(np.concatenate([np.array(edge, dtype=np.int64), rnd.astype(np.int64)]))
+        rows.append(base + sel)
+    return np.concatenate(rows)
+
+
+def oracle_ring_reference(inp, w, rows=None, heads=None):
+    """Oracle result for a ring workload: RoPE (if any) then attention over the
+    whole sequence with the workload's exclusions.  The partition and ring
+    order do not enter: the method reaches the unsplit result."""
+    q, k, v = inp.q.float().cpu(), inp.k.float().cpu(), inp.v.float().cpu()
+    kpm = None if inp.kpm is None else inp.kpm.cpu()
+    am = None if inp.am is None else inp.am.cpu()
+    if heads is not None:
+        # restrict to the listed (b, h) pairs: gather them as a batch of B'=len(heads), H'=1
+        qs = torch.stack([q[b, h] for b, h in heads])[:, None]
+        ks = torch.stack([k[b, h] for b, h in heads])[:, None]
+        vs = torch.stack([v[b, h] for b, h in heads])[:, None]
+        kpm_s = None if kpm is None else torch.stack([kpm[b] for b, _ in heads])
+        q, k, v, kpm = qs, ks, vs, kpm_s
+    if w.rope_base is not None:
+        q = torch.from_numpy(oracle.rope(q, base=w.rope_base, round_to=w.dtype))
+        k = torch.from_numpy(oracle.rope(k, base=w.rope_base, round_to=w.dtype))
+    return oracle.attention(q, k, v, causal=w.causal, kpm=kpm, am=am, rows=rows)

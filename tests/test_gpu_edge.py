@@ -1,0 +1,153 @@
+"""GPU edge cases of the C ABI against the oracle: ragged tails, partial chunks,
+blocks at offsets, accumulate mode and merge, fully masked rows, strided
+(B, T, H, d) inputs, P = 1, empty inputs, bit-exact RoPE and tile classes,
+and the bounded-wait error path."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import blockwise_attention_gb300 as ba
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def rand(shape, dtype, seed, std=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda") * std).to(dtype)
+
+
+DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("bf16", 64), ("bf16", 32), ("bf16", 16), ("f32", 64),
+                                  ("f32", 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_ragged_offsets(dt, d, causal):
+    """Lq, Lk not multiples of 128; the block sits at global offsets."""
+    B, H, Lq, Lk = 2, 3, 300, 333
+    q, k, v = rand((B, H, Lq, d), DT[dt], 1), rand((B, H, Lk, d), DT[dt], 2), rand((B, H, Lk, d), DT[dt], 3)
+    q_off, k_off = 40, 0  # queries 40..339 against keys 0..332
+    out, lse = ba.attn_block_fwd(q, k, v, q_off=q_off, k_off=k_off, causal=causal, out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=causal,
+                                    q_pos0=q_off, k_pos0=k_off)
+    compare(out, lse, o_ref, l_ref, dt, f"block {dt} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("T,P,part", [(1000, 4, "zigzag"), (1000, 4, "contiguous"), (384, 3, "zigzag"),
+                                      (640, 1, "contiguous"), (96, 2, "zigzag")])
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+def test_ring_ragged_chunks(T, P, part, mode):
+    B, H, d = 1, 2, 128
+    q, k, v = rand((B, H, T, d), torch.bfloat16, 4), rand((B, H, T, d), torch.bfloat16, 5), \
+        rand((B, H, T, d), torch.bfloat16, 6)
+    out, lse = ba.ring_attn_fwd(q, k, v, P=P, partition=part, mode=mode, causal=True)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True)
+    compare(out, lse, o_ref, l_ref, "bf16", f"ring T={T} P={P} {part} {mode}")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_accumulate_over_key_blocks_and_merge(dt):
+    """Keys in three blocks folded with accumulate=1, and two halves merged with
+    attn_merge, both equal attention over all keys."""
+    B, H, L, S, d = 2, 2, 200, 390, 64
+    q, k, v = rand((B, H, L, d), DT[dt], 7), rand((B, H, S, d), DT[dt], 8), rand((B, H, S, d), DT[dt], 9)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True, q_pos0=S - L)
+    out = torch.zeros((B, H, L, d), dtype=torch.float32, device="cuda")
+    lse = torch.full((B, H, L), -math.inf, device="cuda")
+    for a, b in [(0, 130), (130, 131), (131, 390)]:   # includes a single-key block
+        ba.attn_block_fwd(q, k[:, :, a:b], v[:, :, a:b], q_off=S - L, k_off=a, causal=True, out=out, lse=lse,
+                          accumulate=True)
+    compare(out, lse, o_ref, l_ref, dt, f"accumulate {dt}")
+    oa, la = ba.attn_block_fwd(q, k[:, :, :256], v[:, :, :256], q_off=S - L, causal=True, out_dtype=torch.float32)
+    ob, lb = ba.attn_block_fwd(q, k[:, :, 256:], v[:, :, 256:], q_off=S - L, k_off=256, causal=True,
+                               out_dtype=torch.float32)
+    ba.attn_merge(oa, la, ob, lb)
+    compare(oa, la, o_ref, l_ref, dt, f"merge {dt}")
+
+
+def test_merge_kernel_against_oracle_merge():
+    g = torch.Generator(device="cuda").manual_seed(3)
+    rows, d = 5000, 128
+    oa = torch.randn((rows, d), generator=g, device="cuda")
+    ob = torch.randn((rows, d), generator=g, device="cuda")
+    la = torch.randn((rows,), generator=g, device="cuda") * 5
+    lb = torch.randn((rows,), generator=g, device="cuda") * 5
+    la[::7] = -math.inf
+    lb[::11] = -math.inf
+    ref_o, ref_l = oracle.merge(oa.cpu().numpy(), la.cpu().numpy(), ob.cpu().numpy(), lb.cpu().numpy())
+    ba.attn_merge(oa, la, ob, lb)
+    l = la.cpu().numpy()
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(fin, np.isfinite(l))
+    assert np.max(np.abs(l[fin] - ref_l[fin])) < 1e-5
+    assert np.max(np.abs(oa.cpu().numpy() - ref_o)) < 1e-5
+
+
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("bf16", 64), ("f32", 32)])
+def test_fully_masked_rows_and_masks(dt, d):
+    B, H, T = 2, 2, 300
+    q, k, v = rand((B, H, T, d), DT[dt], 10), rand((B, H, T, d), DT[dt], 11), rand((B, H, T, d), DT[dt], 12)
+    rng = np.random.default_rng(0)
+    am = (rng.random((T, T)) < 0.3).astype(np.uint8)
+    am[5, :] = 1          # row 5 sees nothing
+    am[200:260, :] = 1    # a band of rows that see nothing
+    am[:, 130:256] = 1    # a fully excluded key tile
+    kpm = np.zeros((B, T), np.uint8)
+    kpm[1, 150:] = 1
+    am_t, kpm_t = torch.from_numpy(am).cuda(), torch.from_numpy(kpm).cuda()
+    out, lse = ba.ring_attn_fwd(q, k, v, P=2, partition="contiguous", attn_mask=am_t, key_padding_mask=kpm_t,
+                                out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), kpm=kpm, am=am)
+    compare(out, lse, o_ref, l_ref, dt, f"masks {dt} d={d}")
+    assert torch.all(out[:, :, 5] == 0) and torch.all(lse[:, :, 5] == -math.inf)
+    cls = ba.tile_classes(B, T, T, key_padding_mask=kpm_t, attn_mask=am_t, causal=True).cpu().numpy()
+    assert np.array_equal(cls, oracle.tile_classes(B, T, T, kpm=kpm, am=am, causal=True))
+
+
+def test_strided_flash_layout():
+    """Q/K/V handed over as (B, T, H, d) storage viewed as (B, H, T, d)."""
+    B, T, H, d = 2, 520, 4, 128
+    base = [rand((B, T, H, d), torch.bfloat16, 20 + i) for i in range(3)]
+    q, k, v = [x.permute(0, 2, 1, 3) for x in base]
+    assert not q.is_contiguous()
+    out, lse = ba.ring_attn_fwd(q, k, v, P=4, partition="zigzag", causal=True)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True)
+    compare(out, lse, o_ref, l_ref, "bf16", "strided")
+
+
+def test_empty_inputs():
+    q = torch.empty((1, 2, 0, 64), dtype=torch.bfloat16, device="cuda")
+    out, lse = ba.ring_attn_fwd(q, q, q, P=1)
+    assert out.numel() == 0 and lse.numel() == 0
+    q = rand((1, 1, 8, 64), torch.bfloat16, 30)
+    kz = torch.empty((1, 1, 0, 64), dtype=torch.bfloat16, device="cuda")
+    out, lse = ba.attn_block_fwd(q, kz, kz, out_dtype=torch.float32)
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_rope_bit_exact(dt):
+    B, H, T, d = 2, 3, 777, 128
+    x = rand((B, H, T, d), DT[dt], 40)
+    y = ba.rope_apply(x, base=10000.0)
+    ref = oracle.rope(x.float().cpu(), base=10000.0, round_to=dt)
+    assert np.array_equal(y.float().cpu().numpy(), ref)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda") * 37 + 5
+    y2 = ba.rope_apply(x, base=500000.0, positions=pos)
+    ref2 = oracle.rope(x.float().cpu(), base=500000.0, positions=pos.cpu().numpy(), round_to=dt)
+    assert np.array_equal(y2.float().cpu().numpy(), ref2)
+
+
+def test_bounded_wait_reports_timeout():
+    assert ba.sync_status() == 0
+    ba.debug_wait_timeout(50_000_000)   # 50 ms on an mbarrier nothing completes
+    assert ba.sync_status() == -4       # BA_ERR_TIMEOUT, context still usable
+    assert ba.sync_status() == 0
+    q = rand((1, 1, 128, 64), torch.bfloat16, 50)
+    out, lse = ba.ring_attn_fwd(q, q, q, P=1)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()

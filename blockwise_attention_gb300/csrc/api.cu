@@ -141,8 +141,12 @@ __global__ void merge_kernel(float *__restrict__ oa, float *__restrict__ la, con
     for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
         const float A = la[r], Bv = lb[r];
         float wa, wb, L;
-        if (Bv == -INFINITY) {
+        if (Bv == -INFINITY && A != -INFINITY) {
             continue;   // nothing to fold in: a unchanged
+        } else if (Bv == -INFINITY) {
+            wa = 0.f;   // neither side saw a key: out = 0, lse = -inf
+            wb = 0.f;
+            L = -INFINITY;
         } else if (A == -INFINITY) {
             wa = 0.f;
             wb = 1.f;

@@ -307,13 +307,21 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tc_fence_after();
                 bool have_prev = false, first_pv = true;
+                // O of the previous item must have been read out before this item
+                // writes O or signals O_FULL.  Waited exactly once per item, so the
+                // O_FULL / O_EMPTY phases never run two ahead of their waiters (an
+                // item without key tiles issues no PV but still commits O_FULL).
+                bool o_free = it_local == 0;
+                auto wait_o_free = [&]() -> bool {
+                    if (o_free) return true;
+                    o_free = true;
+                    return mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim);
+                };
                 auto issue_pv = [&]() -> bool {
                     const uint32_t vs = vcons % C::VS, pb = pcnt & 1;
                     if (!mbar_wait(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort, a.err, lim)) return false;
                     if (!mbar_wait(bar(C::B_PFULL + pb), (pcnt >> 1) & 1, abort, a.err, lim)) return false;
-                    if (first_pv && it_local > 0 &&
-                        !mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim))
-                        return false;
+                    if (first_pv && !wait_o_free()) return false;
                     tc_fence_after();
                     const uint32_t vbase = sV + vs * C::TILE_BYTES;
 #pragma unroll
@@ -362,6 +370,10 @@ __global__ void __launch_bounds__(256, 1)
                 if (!ok) break;
                 mma_commit(bar(C::B_QEMPTY));
                 if (have_prev && !issue_pv()) {
+                    ok = false;
+                    break;
+                }
+                if (!wait_o_free()) {
                     ok = false;
                     break;
                 }

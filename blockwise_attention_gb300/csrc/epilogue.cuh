@@ -14,7 +14,7 @@ namespace ba {
 // A side with -inf carries no keys and gets weight 0.
 __device__ __forceinline__ void merge_weights(float La, float Lb, float &wa, float &wb, float &L) {
     if (Lb == -INFINITY) {
-        wa = 1.f;
+        wa = La == -INFINITY ? 0.f : 1.f;   // both empty: no key at all, out = 0
         wb = 0.f;
         L = La;
         return;

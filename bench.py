@@ -1,7 +1,7 @@
 """Benchmark of the blockwise ring-attention hot path on GB300.
 
 One step = the whole path over one batch of seeded synthetic input:
-RoPE of Q and K (rope_apply x 2) and the fused Ring-Attention kernel
+RoPE of Q and K (one rope_apply launch) and the fused Ring-Attention kernel
 (ring_attn_fwd, P emulated ranks) on the rotated copies, all through the C ABI.
 Default workload: long-context causal prefill, B=1, H=32, T=65536, d=128, bf16,
 RoPE base 10000, P=16 zigzag ranks (the largest single-GPU workload).
@@ -143,23 +143,31 @@ def oracle_cpu_baseline(w, inp_cpu_head, seconds):
     threads = oracle.default_threads()
     rng = np.random.default_rng(0)
 
-    def run(nrows):
-        rows = np.sort(rng.choice(T, size=nrows, replace=False)).astype(np.int64)
-        t0 = time.perf_counter()
-        if w.rope_base is not None:
-            qr = oracle.rope(q, base=w.rope_base, round_to=w.dtype)
-            kr = oracle.rope(k, base=w.rope_base, round_to=w.dtype)
-        else:
-            qr, kr = q, k
-        oracle.attention(qr, kr, v, causal=w.causal, rows=rows, nthreads=threads)
-        dt = time.perf_counter() - t0
-        pairs = int((rows + 1).sum()) if w.causal else nrows * T
-        return dt, pairs
+    def rope_head():
+        if w.rope_base is None:
+            return q, k
+        return (oracle.rope(q, base=w.rope_base, round_to=w.dtype),
+                oracle.rope(k, base=w.rope_base, round_to=w.dtype))
 
-    dt, pairs = run(threads)
-    rate = pairs / max(dt, 1e-6)
-    n = int(min(T, max(threads, threads * round(seconds * rate / (T / 2) / threads))))
-    dt, pairs = run(n)
+    def attend(qr, kr, nrows):
+        rows = np.sort(rng.choice(T, size=nrows, replace=False)).astype(np.int64)
+        oracle.attention(qr, kr, v, causal=w.causal, rows=rows, nthreads=threads)
+        return int((rows + 1).sum()) if w.causal else nrows * T
+
+    # calibrate: RoPE of the head is a fixed cost, attention scales with the rows
+    t0 = time.perf_counter()
+    qr, kr = rope_head()
+    t_rope = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    p_cal = attend(qr, kr, threads)
+    rate = p_cal / max(time.perf_counter() - t0, 1e-6)
+    budget = max(seconds - t_rope, 0.25 * seconds)
+    n = int(min(T, max(threads, threads * round(budget * rate / (T / 2) / threads))))
+    # timed sample: RoPE of the head plus n rows
+    t0 = time.perf_counter()
+    qr, kr = rope_head()
+    pairs = attend(qr, kr, n)
+    dt = time.perf_counter() - t0
     flops = 4.0 * d * pairs
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} random query rows of one head (b=0, h=0) of {w.name}, each over its full "
@@ -222,8 +230,7 @@ def native_arm(args, w, rank, world, local_rank):
         if evs:
             evs[0].record(stream)
         if rope:
-            ba.rope_apply(inp.q, base=w.rope_base, out=qr)
-            ba.rope_apply(inp.k, base=w.rope_base, out=kr)
+            ba.rope_apply(inp.q, x2=inp.k, base=w.rope_base, out=qr, out2=kr)
             q_in, k_in = qr, kr
         else:
             q_in, k_in = inp.q, inp.k
@@ -271,7 +278,7 @@ def native_arm(args, w, rank, world, local_rank):
         total_ms = float(t.item())
     ms_step = total_ms / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
-    kernels_per_step = (2 if rope else 0) + (1 if args.mode == "fused" else w.P) + \
+    kernels_per_step = (1 if rope else 0) + (1 if args.mode == "fused" else w.P) + \
         (1 if (inp.kpm is not None or inp.am is not None) else 0)
 
     # end to end through the one-call API with host buffers

@@ -121,7 +121,7 @@ def load(path: str | None = None):
     lib.ring_attn_fwd.argtypes = [T, T, T, i, i, i, i, i, i, i, i, vp, i64, vp, i64, i, f, i, f, vp, i, vp, vp,
                                   vp, sz, vp]
     lib.rope_apply.restype = i
-    lib.rope_apply.argtypes = [T, i, i, i, i, i, vp, f, vp, vp]
+    lib.rope_apply.argtypes = [T, T, i, i, i, i, i, vp, f, vp, vp, vp]
     lib.ba_tile_classes.restype = i
     lib.ba_tile_classes.argtypes = [i, i, i, i64, i64, vp, i64, vp, i64, i, vp, vp]
     lib.ba_index_maps.restype = i
@@ -261,17 +261,24 @@ def ring_attn_fwd(q, k, v, *, P, partition="contiguous", mode="fused", key_paddi
     return out, lse
 
 
-def rope_apply(x, *, base=10000.0, positions=None, out=None, stream=None):
-    """Rotary position embedding of x (B, H, T, d) into a contiguous output."""
+def rope_apply(x, *, x2=None, base=10000.0, positions=None, out=None, out2=None, stream=None):
+    """Rotary position embedding of x (B, H, T, d) into a contiguous output; with
+    x2 given, rotates x2 by the same launch and returns (y, y2)."""
     lib = load()
     B, H, T, d = x.shape
     if out is None:
         out = torch.empty((B, H, T, d), dtype=x.dtype, device=x.device)
+    if x2 is not None:
+        if x2.shape != x.shape or x2.dtype != x.dtype:
+            raise ValueError("x2 must match x")
+        if out2 is None:
+            out2 = torch.empty((B, H, T, d), dtype=x.dtype, device=x.device)
     if positions is not None and (positions.dtype != torch.int32 or not positions.is_cuda):
         raise ValueError("positions: int32 CUDA tensor")
-    _check("rope_apply", lib.rope_apply(_tensor(x), B, H, T, d, _dtype_code(x.dtype), _ptr(positions),
-                                        float(base), _ptr(out), _stream(stream)))
-    return out
+    t2 = _tensor(x2) if x2 is not None else ba_tensor(None, 0, 0, 0)
+    _check("rope_apply", lib.rope_apply(_tensor(x), t2, B, H, T, d, _dtype_code(x.dtype), _ptr(positions),
+                                        float(base), _ptr(out), _ptr(out2), _stream(stream)))
+    return out if x2 is None else (out, out2)
 
 
 def tile_classes(B, Lq, Lk, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None, causal=False,

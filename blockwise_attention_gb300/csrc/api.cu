@@ -182,6 +182,17 @@ struct Thetas {
     double th[64];
 };
 
+// Up to two tensors rotated by one launch (Q and K share the angles).
+struct RopeArgs {
+    const void *x[2];
+    long long sB[2], sH[2], sT[2];
+    void *y[2];
+    int n;
+    int B, H, T, d;
+    const int32_t *positions;
+    Thetas th;
+};
+
 // fp64 -> bf16 with one rounding (ties to even): truncate to fp32, make the
 // result's last bit sticky when inexact (round-to-odd), then round to bf16.
 __device__ __forceinline__ __nv_bfloat16 round_bf16_from_f64(double y) {
@@ -190,39 +201,171 @@ __device__ __forceinline__ __nv_bfloat16 round_bf16_from_f64(double y) {
     return __float2bfloat16_rn(f);
 }
 
-template <typename T>
-__device__ __forceinline__ double ld(const T *p);
-template <>
-__device__ __forceinline__ double ld<float>(const float *p) { return (double)*p; }
-template <>
-__device__ __forceinline__ double ld<__nv_bfloat16>(const __nv_bfloat16 *p) {
-    return (double)__bfloat162float(*p);
+// Error-free sum of two floats (Knuth): a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
-__device__ __forceinline__ void st(float *p, double y) { *p = __double2float_rn(y); }
-__device__ __forceinline__ void st(__nv_bfloat16 *p, double y) { *p = round_bf16_from_f64(y); }
 
-// One thread per (position t, pair c); the angle's cos/sin are computed once
-// and applied to that pair in every (b, h).
-template <typename T>
-__global__ void rope_kernel(const T *__restrict__ x, long long sB, long long sH, long long sT, int B, int H, int Tn,
-                            int d, const int32_t *__restrict__ positions, const Thetas th, T *__restrict__ y) {
-    const int half = d / 2;
-    const long long n = (long long)Tn * half;
+// A double split into four floats of at most 16 significant bits each
+// (c ~= k0 + k1 + k2 + k3, relative error below 2^-48), so that the product
+// of any piece with a bfloat16 value (8 significant bits) is exact in fp32.
+struct Split4 {
+    float k[4];
+};
+__device__ __forceinline__ Split4 split16(double c) {
+    Split4 r;
+    double rem = c;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const float f = __uint_as_float(__float_as_uint(__double2float_rn(rem)) & 0xFFFFFF00u);
+        r.k[i] = f;
+        rem -= (double)f;
+    }
+    r.k[3] = __double2float_rn(rem);
+    return r;
+}
+
+// x0 * c - x1 * s (or x0 * s + x1 * c with the roles passed in) for bfloat16
+// x0, x1, rounded once to bfloat16.  Level-1 and level-2 products are exact
+// and summed with error-free transforms; the rest carries < 2^-47 |x|.
+__device__ __forceinline__ uint16_t rot_bf16(float x0, const Split4 &a, float x1, const Split4 &b) {
+    // y = x0 * a - x1 * b
+    float h1, l1, h2, l2;
+    two_sum(__fmul_rn(x0, a.k[0]), -__fmul_rn(x1, b.k[0]), h1, l1);
+    two_sum(__fmul_rn(x0, a.k[1]), -__fmul_rn(x1, b.k[1]), h2, l2);
+    const float t3 = __fsub_rn(__fmul_rn(x0, a.k[2]), __fmul_rn(x1, b.k[2]));
+    const float t4 = __fsub_rn(__fmul_rn(x0, a.k[3]), __fmul_rn(x1, b.k[3]));
+    float s, e;
+    two_sum(h1, h2, s, e);
+    const float small = __fadd_rn(__fadd_rn(__fadd_rn(l1, l2), __fadd_rn(t3, t4)), e);
+    float hi, lo;
+    two_sum(s, small, hi, lo);               // hi + lo = value, |lo| <= ulp(hi) / 2
+    // Round hi + lo to bfloat16: only when hi sits exactly on a bfloat16
+    // midpoint does lo decide the direction.
+    const uint32_t u = __float_as_uint(hi);
+    uint32_t bits;
+    if ((u & 0xFFFFu) == 0x8000u && lo != 0.f) {
+        const bool away = (lo > 0.f) == (hi > 0.f);
+        bits = away ? (u + 0x8000u) >> 16 : u >> 16;
+    } else {
+        bits = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    }
+    return (uint16_t)bits;
+}
+
+// bfloat16, 8 elements (4 pairs) per thread per head: one thread per
+// (position t, 4 consecutive pairs); the angles' cos/sin are computed once in
+// fp64 and applied to those pairs in every tensor and (b, h).
+template <bool VEC>
+__global__ void rope_bf16_kernel(const RopeArgs a) {
+    const int groups = a.d / 8;
+    const long long n = (long long)a.T * groups;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(e / groups), c0 = (int)(e % groups) * 4;
+        const double m = a.positions ? (double)a.positions[t] : (double)t;
+        Split4 cs[4], sn[4], nsn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            double sv, cv;
+            sincos(m * a.th.th[c0 + i], &sv, &cv);
+            cs[i] = split16(cv);
+            sn[i] = split16(sv);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) nsn[i].k[k] = -sn[i].k[k];
+        }
+        for (int ti = 0; ti < a.n; ++ti) {
+            const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(a.x[ti]);
+            __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(a.y[ti]);
+            for (int b = 0; b < a.B; ++b) {
+                for (int h = 0; h < a.H; ++h) {
+                    const __nv_bfloat16 *px = xb + b * a.sB[ti] + h * a.sH[ti] + (long long)t * a.sT[ti] + 2 * c0;
+                    uint16_t in[8], out[8];
+                    if (VEC) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(px);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            in[2 * i] = (uint16_t)(w[i] & 0xFFFFu);
+                            in[2 * i + 1] = (uint16_t)(w[i] >> 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) in[i] = __bfloat16_as_ushort(px[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x0 = __uint_as_float((uint32_t)in[2 * i] << 16);
+                        const float x1 = __uint_as_float((uint32_t)in[2 * i + 1] << 16);
+                        out[2 * i] = rot_bf16(x0, cs[i], x1, sn[i]);        // x0 cos - x1 sin
+                        out[2 * i + 1] = rot_bf16(x0, sn[i], x1, nsn[i]);   // x0 sin + x1 cos
+                    }
+                    __nv_bfloat16 *py = yb + (((long long)b * a.H + h) * a.T + t) * a.d + 2 * c0;
+                    uint4 o;
+                    o.x = out[0] | ((uint32_t)out[1] << 16);
+                    o.y = out[2] | ((uint32_t)out[3] << 16);
+                    o.z = out[4] | ((uint32_t)out[5] << 16);
+                    o.w = out[6] | ((uint32_t)out[7] << 16);
+                    *reinterpret_cast<uint4 *>(py) = o;
+                }
+            }
+        }
+    }
+}
+
+// float32 (and any layout): fp64 arithmetic, one thread per (position, pair).
+__global__ void rope_f32_kernel(const RopeArgs a) {
+    const int half = a.d / 2;
+    const long long n = (long long)a.T * half;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e / half), c = (int)(e % half);
-        const double m = positions ? (double)positions[t] : (double)t;
+        const double m = a.positions ? (double)a.positions[t] : (double)t;
         double sn, cs;
-        sincos(m * th.th[c], &sn, &cs);
-        for (int b = 0; b < B; ++b) {
-            for (int h = 0; h < H; ++h) {
-                const T *px = x + b * sB + h * sH + t * sT + 2 * c;
-                const double x0 = ld(px), x1 = ld(px + 1);
-                const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
-                const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
-                T *py = y + (((long long)b * H + h) * Tn + t) * d + 2 * c;
-                st(py, y0);
-                st(py + 1, y1);
+        sincos(m * a.th.th[c], &sn, &cs);
+        for (int ti = 0; ti < a.n; ++ti) {
+            const float *xb = static_cast<const float *>(a.x[ti]);
+            float *yb = static_cast<float *>(a.y[ti]);
+            for (int b = 0; b < a.B; ++b) {
+                for (int h = 0; h < a.H; ++h) {
+                    const float *px = xb + b * a.sB[ti] + h * a.sH[ti] + (long long)t * a.sT[ti] + 2 * c;
+                    const double x0 = px[0], x1 = px[1];
+                    const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
+                    const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
+                    float *py = yb + (((long long)b * a.H + h) * a.T + t) * a.d + 2 * c;
+                    py[0] = __double2float_rn(y0);
+                    py[1] = __double2float_rn(y1);
+                }
+            }
+        }
+    }
+}
+
+// bfloat16 with a head dimension that is not a multiple of 8: fp64, per pair.
+__global__ void rope_bf16_pair_kernel(const RopeArgs a) {
+    const int half = a.d / 2;
+    const long long n = (long long)a.T * half;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(e / half), c = (int)(e % half);
+        const double m = a.positions ? (double)a.positions[t] : (double)t;
+        double sn, cs;
+        sincos(m * a.th.th[c], &sn, &cs);
+        for (int ti = 0; ti < a.n; ++ti) {
+            const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(a.x[ti]);
+            __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(a.y[ti]);
+            for (int b = 0; b < a.B; ++b) {
+                for (int h = 0; h < a.H; ++h) {
+                    const __nv_bfloat16 *px = xb + b * a.sB[ti] + h * a.sH[ti] + (long long)t * a.sT[ti] + 2 * c;
+                    const double x0 = __bfloat162float(px[0]), x1 = __bfloat162float(px[1]);
+                    const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
+                    const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
+                    __nv_bfloat16 *py = yb + (((long long)b * a.H + h) * a.T + t) * a.d + 2 * c;
+                    py[0] = round_bf16_from_f64(y0);
+                    py[1] = round_bf16_from_f64(y1);
+                }
             }
         }
     }
@@ -279,22 +422,43 @@ int run_tile_classes(const Geom &g, int8_t *cls, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
-int launch_rope(const ba_tensor &x, int B, int H, int T, int d, int dtype, const int32_t *pos, float base, void *y,
-                cudaStream_t s) {
-    Thetas th;
-    for (int c = 0; c < d / 2; ++c) th.th[c] = std::pow((double)base, -(double)(2 * c) / (double)d);
-    const long long n = (long long)T * (d / 2);
-    if (n == 0 || B == 0 || H == 0) return BA_OK;
+// Rotate one or two (B, H, T, d) tensors (x2 / y2 may be null) into contiguous outputs.
+int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, int d, int dtype,
+                const int32_t *pos, float base, void *y, void *y2, cudaStream_t s) {
+    RopeArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int c = 0; c < d / 2; ++c) a.th.th[c] = std::pow((double)base, -(double)(2 * c) / (double)d);
+    a.n = x2 ? 2 : 1;
+    const ba_tensor *xs[2] = {&x, x2};
+    void *ys[2] = {y, y2};
+    bool vec = dtype == BA_BF16 && d % 8 == 0;
+    for (int i = 0; i < a.n; ++i) {
+        a.x[i] = xs[i]->ptr;
+        a.sB[i] = xs[i]->sB;
+        a.sH[i] = xs[i]->sH;
+        a.sT[i] = xs[i]->sT;
+        a.y[i] = ys[i];
+        vec = vec && reinterpret_cast<uintptr_t>(a.x[i]) % 16 == 0 && reinterpret_cast<uintptr_t>(a.y[i]) % 16 == 0 &&
+              a.sT[i] % 8 == 0 && (H <= 1 || a.sH[i] % 8 == 0) && (B <= 1 || a.sB[i] % 8 == 0);
+    }
+    a.B = B;
+    a.H = H;
+    a.T = T;
+    a.d = d;
+    a.positions = pos;
+    if ((long long)T * d == 0 || B == 0 || H == 0) return BA_OK;
     const int threads = 256;
-    long long blocks = (n + threads - 1) / threads;
+    const long long per = dtype == BA_BF16 && d % 8 == 0 ? d / 8 : d / 2;
+    long long blocks = ((long long)T * per + threads - 1) / threads;
     if (blocks > 1 << 20) blocks = 1 << 20;
-    if (dtype == BA_BF16)
-        rope_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(x.ptr), x.sB, x.sH, x.sT, B, H, T, d, pos, th,
-            static_cast<__nv_bfloat16 *>(y));
+    if (dtype == BA_F32)
+        rope_f32_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
+    else if (d % 8 != 0)
+        rope_bf16_pair_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
+    else if (vec)
+        rope_bf16_kernel<true><<<(unsigned)blocks, threads, 0, s>>>(a);
     else
-        rope_kernel<float><<<(unsigned)blocks, threads, 0, s>>>(static_cast<const float *>(x.ptr), x.sB, x.sH,
-                                                                 x.sT, B, H, T, d, pos, th, static_cast<float *>(y));
+        rope_bf16_kernel<false><<<(unsigned)blocks, threads, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -404,16 +568,17 @@ int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
-int rope_apply(ba_tensor x, int B, int H, int T, int d, int dtype, const int32_t *positions, float base, void *y,
-               ba_stream_t stream) {
-    if (!x.ptr || !y || B < 0 || H < 0 || T < 0 || d < 2 || (d & 1) || d > 128 || !valid_dtype(dtype) ||
-        !(base > 0.f))
+int rope_apply(ba_tensor x, ba_tensor x2, int B, int H, int T, int d, int dtype, const int32_t *positions,
+               float base, void *y, void *y2, ba_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || d < 2 || (d & 1) || d > 128 || !valid_dtype(dtype) || !(base > 0.f))
         return BA_ERR_ARG;
+    const bool two = x2.ptr != nullptr || y2 != nullptr;
+    if ((long long)B * H * T > 0 && (!x.ptr || !y || (two && (!x2.ptr || !y2)))) return BA_ERR_ARG;
     const int dev = current_device();
     if (dev < 0) return BA_ERR_CUDA;
     int rc = device_setup(dev);
     if (rc) return rc;
-    return launch_rope(x, B, H, T, d, dtype, positions, base, y, stream);
+    return launch_rope(x, two ? &x2 : nullptr, B, H, T, d, dtype, positions, base, y, two ? y2 : nullptr, stream);
 }
 
 int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off, const uint8_t *key_padding_mask,
@@ -605,8 +770,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
         wp += align256(tensor * elem_size(dtype));
         void *kr = wp;
         wp += align256(tensor * elem_size(dtype));
-        if ((rc = launch_rope(q, B, H, T, d, dtype, nullptr, rope_base, qr, stream))) return rc;
-        if ((rc = launch_rope(k, B, H, T, d, dtype, nullptr, rope_base, kr, stream))) return rc;
+        if ((rc = launch_rope(q, &k, B, H, T, d, dtype, nullptr, rope_base, qr, kr, stream))) return rc;
         const long long sT = d, sH = (long long)T * d, sB = (long long)H * T * d;
         q = ba_tensor{qr, sB, sH, sT};
         k = ba_tensor{kr, sB, sH, sT};

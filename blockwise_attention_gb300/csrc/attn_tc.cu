@@ -172,6 +172,41 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
+// 32 bytes of an exclusion mask (1 = excluded) starting at p, of which the
+// first n are meaningful, applied to s[0..31].
+__device__ __forceinline__ void mask_bytes(const uint8_t *p, int n, float *s) {
+    uint32_t w[8];
+    if (n >= 32 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p + 16));
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = 0;
+        for (int i = 0; i < n && i < 32; ++i) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if ((w[i >> 2] >> (8 * (i & 3))) & 0xffu) s[i] = -INFINITY;
+}
+
+// Exclusions of keys [c0, c0 + 32) of key tile kt for the query at global
+// position qpos: past the tile end, causal future, key padding, attn_mask.
+__device__ __forceinline__ void mask_chunk(const Geom &g, int b, long long qpos, bool row_valid, const KTile &kt,
+                                           int c0, float *s) {
+    const long long diag = qpos - kt.pos0;   // key j lies in the future when j > diag
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int j = c0 + i;
+        if (j >= kt.len || (g.causal && j > diag)) s[i] = -INFINITY;
+    }
+    const int n = kt.len - c0;
+    if (!row_valid || n <= 0) return;
+    if (g.kpm) mask_bytes(g.kpm + b * g.kpm_ld + kt.pos0 + c0, n, s);
+    if (g.am) mask_bytes(g.am + qpos * g.am_ld + kt.pos0 + c0, n, s);
+}
+
 // ----------------------------------------------------------------------------
 // Kernel
 // ----------------------------------------------------------------------------
@@ -409,30 +444,32 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tc_fence_after();
                 float s[TILE];
+                {
+                    uint32_t r[TILE];
 #pragma unroll
-                for (int c = 0; c < TILE / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32, r);
+                    for (int c = 0; c < TILE / 32; ++c)
+                        tmem_ld32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32,
+                                  *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                    for (int j = 0; j < TILE; ++j) s[j] = __uint_as_float(r[j]);
                 }
                 tc_fence_before();
                 mbar_arrive(bar(C::B_SEMPTY + sb));
 
-                const bool need_mask = kt.cls == BA_TILE_PARTIAL || kt.len < TILE;
-                const bool row_valid = row < qt.len;   // rows past the tile end are never stored
-                float mx = -INFINITY;
-                if (need_mask) {
+                if (kt.cls == BA_TILE_PARTIAL || kt.len < TILE) {
+                    const bool row_valid = row < qt.len;   // rows past the tile end are never stored
 #pragma unroll
-                    for (int j = 0; j < TILE; ++j) {
-                        if (j >= kt.len || (row_valid && excluded(g, qt.b, qpos, kt.pos0 + j))) s[j] = -INFINITY;
-                        mx = fmaxf(mx, s[j]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < TILE; ++j) mx = fmaxf(mx, s[j]);
+                    for (int c = 0; c < TILE / 32; ++c) mask_chunk(g, qt.b, qpos, row_valid, kt, c * 32, &s[c * 32]);
                 }
+                // row maximum: 8 independent chains, then a tree
+                float mc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mc[k] = s[k];
+#pragma unroll
+                for (int j = 8; j < TILE; ++j) mc[j & 7] = fmaxf(mc[j & 7], s[j]);
+                const float mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
+                                       fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool resc = m_new > m_ref + 8.0f;   // true when m_ref = -inf and m_new finite
                 float alpha = 1.f;
@@ -441,15 +478,18 @@ __global__ void __launch_bounds__(256, 1)
                     m_ref = m_new;
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                float sum = 0.f;
+                float sc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) sc[k] = 0.f;
                 uint32_t pk[TILE / 2];
 #pragma unroll
                 for (int j = 0; j < TILE / 2; ++j) {
                     const float p0 = fast_exp2(fmaf(s[2 * j], sl2, -m_use));
                     const float p1 = fast_exp2(fmaf(s[2 * j + 1], sl2, -m_use));
-                    sum += p0 + p1;
+                    sc[j & 7] += p0 + p1;
                     pk[j] = pack_bf16(p0, p1);
                 }
+                const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;
 
                 const uint32_t pb = scnt & 1;
@@ -459,12 +499,9 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < TILE / 64; ++c) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = pk[c * 32 + i];
-                    tmem_st32(tmem + lane_addr + C::P_COL + pb * 64 + c * 32, r);
-                }
+                for (int c = 0; c < TILE / 64; ++c)
+                    tmem_st32(tmem + lane_addr + C::P_COL + pb * 64 + c * 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
                     const uint32_t prev = scnt - 1;
                     if (!warp_wait(bar(C::B_PVDONE + (prev & 1)), (prev >> 1) & 1, abort, a.err, lim)) {

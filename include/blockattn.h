@@ -157,14 +157,18 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v,
  * rope_apply -- rotary position embedding ("RoFormer", item #4 of ai.engineer
  * "Transformers and Attention"): split each d-vector into coordinate pairs
  * (2c, 2c+1) and rotate pair c by the angle m * base^(-2c/d), m the token
- * position: (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).  The rotation is
- * evaluated in fp64 and rounded once (ties to even) to the tensor dtype.
+ * position: (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos).  The result equals
+ * the rotation evaluated in fp64 and rounded once (ties to even) to the
+ * tensor dtype (bf16 uses exact fp32 products of 16-bit pieces of the fp64
+ * cos/sin, summed with error-free transforms).
  *  x: (B, H, T, d) strided input; y: (B, H, T, d) contiguous output of the
- *  same dtype (may not alias x).  positions: NULL (position of row t is t)
- *  or device int32[T].  d must be even (else BA_ERR_ARG).
+ *  same dtype (may not alias x).  x2 / y2: an optional second tensor of the
+ *  same shape rotated by the same launch (e.g. K next to Q); pass
+ *  x2.ptr = NULL and y2 = NULL for one tensor.  positions: NULL (position of
+ *  row t is t) or device int32[T].  d must be even and <= 128 (else BA_ERR_ARG).
  */
-int rope_apply(ba_tensor x, int B, int H, int T, int d, int dtype,
-               const int32_t *positions, float base, void *y, ba_stream_t stream);
+int rope_apply(ba_tensor x, ba_tensor x2, int B, int H, int T, int d, int dtype,
+               const int32_t *positions, float base, void *y, void *y2, ba_stream_t stream);
 
 /*
  * ba_tile_classes -- class of each 128 x 128 tile of the combined exclusion

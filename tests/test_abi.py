@@ -73,7 +73,7 @@ def test_argument_errors_are_host_side():
     assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 12, 64, 1, 4, 1, 1, None, 0, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
                              dummy, None, None, 0, None) == _lib.BA_ERR_SHAPE
     # ring: odd d with rope
-    assert lib.rope_apply(T1, 1, 1, 8, 7, 1, None, 1e4, dummy, None) == _lib.BA_ERR_ARG
+    assert lib.rope_apply(T1, T0, 1, 1, 8, 7, 1, None, 1e4, dummy, None, None) == _lib.BA_ERR_ARG
     assert lib.attn_merge(None, dummy, dummy, dummy, 4, 4, None) == _lib.BA_ERR_ARG
 
 

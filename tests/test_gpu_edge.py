@@ -129,17 +129,31 @@ def test_empty_inputs():
     assert torch.all(out == 0) and torch.all(lse == -math.inf)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_rope_bit_exact(dt):
-    B, H, T, d = 2, 3, 777, 128
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("bf16", 64), ("bf16", 16), ("bf16", 6), ("f32", 128),
+                                  ("f32", 10)])
+def test_rope_bit_exact(dt, d):
+    B, H, T = 2, 3, 777
     x = rand((B, H, T, d), DT[dt], 40)
+    x2 = rand((B, H, T, d), DT[dt], 41, std=3.0)
     y = ba.rope_apply(x, base=10000.0)
     ref = oracle.rope(x.float().cpu(), base=10000.0, round_to=dt)
     assert np.array_equal(y.float().cpu().numpy(), ref)
     pos = torch.arange(T, dtype=torch.int32, device="cuda") * 37 + 5
-    y2 = ba.rope_apply(x, base=500000.0, positions=pos)
-    ref2 = oracle.rope(x.float().cpu(), base=500000.0, positions=pos.cpu().numpy(), round_to=dt)
-    assert np.array_equal(y2.float().cpu().numpy(), ref2)
+    y1, y2 = ba.rope_apply(x, x2=x2, base=500000.0, positions=pos)
+    for xi, yi in ((x, y1), (x2, y2)):
+        ref2 = oracle.rope(xi.float().cpu(), base=500000.0, positions=pos.cpu().numpy(), round_to=dt)
+        assert np.array_equal(yi.float().cpu().numpy(), ref2)
+
+
+def test_rope_strided_and_large_positions():
+    """Strided (B, T, H, d) input; positions up to 2^20, where angles are large."""
+    B, T, H, d = 1, 300, 4, 128
+    base = rand((B, T, H, d), torch.bfloat16, 42)
+    x = base.permute(0, 2, 1, 3)
+    pos = torch.randint(0, 1 << 20, (T,), dtype=torch.int32, device="cuda")
+    y = ba.rope_apply(x, base=10000.0, positions=pos)
+    ref = oracle.rope(x.float().cpu(), base=10000.0, positions=pos.cpu().numpy(), round_to="bf16")
+    assert np.array_equal(y.float().cpu().numpy(), ref)
 
 
 def test_bounded_wait_reports_timeout():

@@ -60,8 +60,7 @@ def test_zigzag_prefill_64k_rope_bench_launch():
     RoPE on Q and K, then the fused ring kernel on the rotated copies."""
     w = WORKLOADS["zigzag_prefill_64k_rope"]
     inp = make_inputs(w, "cuda")
-    qr = ba.rope_apply(inp.q, base=w.rope_base)
-    kr = ba.rope_apply(inp.k, base=w.rope_base)
+    qr, kr = ba.rope_apply(inp.q, x2=inp.k, base=w.rope_base)
     out, lse = ba.ring_attn_fwd(qr, kr, inp.v, P=w.P, partition=w.partition, mode="fused", causal=True)
     heads = [(0, 0), (0, 13), (0, 31)]
     rows_r = sample_rows(len(heads), 1, w.T, [(i, 0) for i in range(len(heads))], 160, w.T // (2 * w.P))
@@ -73,9 +72,10 @@ def test_zigzag_prefill_64k_rope_bench_launch():
     out2, lse2 = run_ring(w, inp, "fused")
     assert torch.equal(out2, out) and torch.equal(lse2, lse)
     # rotated heads equal the oracle's rotation bit for bit
-    for b, h in heads[:1]:
-        ref = oracle.rope(inp.q[b, h].float().cpu(), base=w.rope_base, round_to="bf16")
-        assert np.array_equal(qr[b, h].float().cpu().numpy(), ref)
+    for b, h in heads[:2]:
+        for x, xr in ((inp.q, qr), (inp.k, kr)):
+            ref = oracle.rope(x[b, h].float().cpu(), base=w.rope_base, round_to="bf16")
+            assert np.array_equal(xr[b, h].float().cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("mode", ["fused", "stepwise"])

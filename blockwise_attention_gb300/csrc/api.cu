@@ -266,7 +266,7 @@ __global__ void rope_bf16_kernel(const RopeArgs a) {
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e / groups), c0 = (int)(e % groups) * 4;
         const double m = a.positions ? (double)a.positions[t] : (double)t;
-        Split4 cs[4], sn[4], nsn[4];
+        Split4 cs[4], sn[4], ncs[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             double sv, cv;
@@ -274,7 +274,7 @@ __global__ void rope_bf16_kernel(const RopeArgs a) {
             cs[i] = split16(cv);
             sn[i] = split16(sv);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) nsn[i].k[k] = -sn[i].k[k];
+            for (int k = 0; k < 4; ++k) ncs[i].k[k] = -cs[i].k[k];
         }
         for (int ti = 0; ti < a.n; ++ti) {
             const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(a.x[ti]);
@@ -300,7 +300,7 @@ __global__ void rope_bf16_kernel(const RopeArgs a) {
                         const float x0 = __uint_as_float((uint32_t)in[2 * i] << 16);
                         const float x1 = __uint_as_float((uint32_t)in[2 * i + 1] << 16);
                         out[2 * i] = rot_bf16(x0, cs[i], x1, sn[i]);        // x0 cos - x1 sin
-                        out[2 * i + 1] = rot_bf16(x0, sn[i], x1, nsn[i]);   // x0 sin + x1 cos
+                        out[2 * i + 1] = rot_bf16(x0, sn[i], x1, ncs[i]);   // x0 sin - x1 (-cos)
                     }
                     __nv_bfloat16 *py = yb + (((long long)b * a.H + h) * a.T + t) * a.d + 2 * c0;
                     uint4 o;

@@ -45,10 +45,10 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
     }
     float m = -INFINITY, l = 0.f;   // running max (log2 units) and denominator
 
-    const int nwalk = walk_length(g);
-    for (int it = 0; it < nwalk; ++it) {
-        const KTile kt = walk_tile(g, qt, it);
-        if (kt.cls == BA_TILE_EMPTY) continue;
+    KWalk wk;
+    kwalk_begin(g, qt, wk);
+    KTile kt;
+    while (kwalk_next(g, qt, wk, kt)) {
         for (int s0 = 0; s0 < kt.len; s0 += SUB) {
             __syncthreads();
             for (int e = threadIdx.x; e < SUB * D; e += blockDim.x) {

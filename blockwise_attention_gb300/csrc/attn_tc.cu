@@ -34,6 +34,11 @@
 namespace ba {
 namespace {
 
+// PV of key tile j is issued after QK of tile j + PV_LAG.  With two S and two
+// P buffers in TMEM, a lag of 1 keeps one QK queued behind every PV (a lag of 2
+// measured no better on the 8K and 64K causal workloads).
+constexpr int PV_LAG = 1;
+
 template <int D>
 struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
@@ -270,7 +275,6 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int nwalk = walk_length(g);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -287,9 +291,10 @@ __global__ void __launch_bounds__(256, 1)
                 for (int bx = 0; bx < C::NBOX; ++bx)
                     tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, qt.row0, qt.h, qt.b, bar(C::B_QFULL));
                 ++qfills;
-                for (int it = 0; it < nwalk; ++it) {
-                    const KTile kt = walk_tile(g, qt, it);
-                    if (kt.cls == BA_TILE_EMPTY) continue;
+                KWalk wk;
+                kwalk_begin(g, qt, wk);
+                KTile kt;
+                while (kwalk_next(g, qt, wk, kt)) {
                     uint32_t st = kfill % C::KS, use = kfill / C::KS;
                     if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
                         ok = false;
@@ -341,7 +346,8 @@ __global__ void __launch_bounds__(256, 1)
                     break;
                 }
                 tc_fence_after();
-                bool have_prev = false, first_pv = true;
+                bool first_pv = true;
+                uint32_t pending = 0;   // tiles whose QK is issued but whose PV is not yet
                 // O of the previous item must have been read out before this item
                 // writes O or signals O_FULL.  Waited exactly once per item, so the
                 // O_FULL / O_EMPTY phases never run two ahead of their waiters (an
@@ -369,12 +375,14 @@ __global__ void __launch_bounds__(256, 1)
                     mma_commit(bar(C::B_PVDONE + pb));
                     ++vcons;
                     ++pcnt;
+                    --pending;
                     first_pv = false;
                     return true;
                 };
-                for (int it = 0; it < nwalk && ok; ++it) {
-                    const KTile kt = walk_tile(g, qt, it);
-                    if (kt.cls == BA_TILE_EMPTY) continue;
+                KWalk wk;
+                kwalk_begin(g, qt, wk);
+                KTile kt;
+                while (ok && kwalk_next(g, qt, wk, kt)) {
                     const uint32_t ks = kcons % C::KS, sb = scnt & 1;
                     if (!mbar_wait(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort, a.err, lim)) {
                         ok = false;
@@ -396,18 +404,23 @@ __global__ void __launch_bounds__(256, 1)
                     mma_commit(bar(C::B_KEMPTY + ks));
                     ++kcons;
                     ++scnt;
-                    if (have_prev && !issue_pv()) {
+                    ++pending;
+                    // PV of tile j - PV_LAG follows QK of tile j, so the tensor pipe has
+                    // QK work queued while the softmax of the lagging tiles runs.
+                    if (pending > (uint32_t)PV_LAG && !issue_pv()) {
                         ok = false;
                         break;
                     }
-                    have_prev = true;
                 }
                 if (!ok) break;
                 mma_commit(bar(C::B_QEMPTY));
-                if (have_prev && !issue_pv()) {
-                    ok = false;
-                    break;
+                while (pending > 0) {
+                    if (!issue_pv()) {
+                        ok = false;
+                        break;
+                    }
                 }
+                if (!ok) break;
                 if (!wait_o_free()) {
                     ok = false;
                     break;
@@ -434,9 +447,10 @@ __global__ void __launch_bounds__(256, 1)
             const long long qpos = qt.pos0 + row;
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;
-            for (int it = 0; it < nwalk; ++it) {
-                const KTile kt = walk_tile(g, qt, it);
-                if (kt.cls == BA_TILE_EMPTY) continue;
+            KWalk wk;
+            kwalk_begin(g, qt, wk);
+            KTile kt;
+            while (kwalk_next(g, qt, wk, kt)) {
                 const uint32_t sb = scnt & 1;
                 if (!warp_wait(bar(C::B_SFULL + sb), (scnt >> 1) & 1, abort, a.err, lim)) {
                     ok = false;

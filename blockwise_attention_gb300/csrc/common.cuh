@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/blockattn.h"
+#include "blockattn.h"
 
 namespace ba {
 
@@ -131,30 +131,80 @@ __host__ __device__ inline int causal_class(const QTile &q, const KTile &k) {
     return BA_TILE_PARTIAL;
 }
 
-// it-th key tile of the walk of query tile q, with its class.
-__device__ inline KTile walk_tile(const Geom &g, const QTile &q, int it) {
-    int kg;
+// Incremental walk over the key tiles a query tile visits, in ring order,
+// with EMPTY tiles skipped.  Every role of a kernel runs the same walk, so they
+// agree on the sequence without communicating.  Without a class map, causal
+// EMPTY tiles are skipped chunk-wise (a key tile, and every later tile of its
+// chunk, is EMPTY once its first key lies after the query tile's last row).
+struct KWalk {
+    int s;       // ring step (ring mode)
+    int ci;      // chunk of the source rank, in its local order (ring mode)
+    int t;       // tile within the chunk
+    int c;       // global chunk id
+    int n_ch;    // chunks per rank
+    int src;     // source rank of step s
+};
+
+__host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile &q, KWalk &w) {
+    w.t = 0;
+    w.ci = 0;
     if (g.ring) {
-        int per_rank = (g.zigzag ? 2 : 1) * g.nkt_pc;
-        int s = g.s_begin + it / per_rank;
-        int rem = it % per_rank;
-        int src = q.rank - s;
-        src = ((src % g.P) + g.P) % g.P;
-        int ci = rem / g.nkt_pc;               // which of src's chunks (local order)
-        int c = ci == 0 ? src : 2 * g.P - 1 - src;
-        kg = c * g.nkt_pc + rem % g.nkt_pc;
+        w.s = g.s_begin;
+        w.n_ch = g.zigzag ? 2 : 1;
+        w.src = ((q.rank - w.s) % g.P + g.P) % g.P;
+        w.c = w.src;
     } else {
-        kg = it;
+        w.s = 0;
+        w.n_ch = 1;
+        w.src = 0;
+        w.c = 0;
     }
-    KTile k = k_tile_by_id(g, kg);
-    if (g.cls) {
-        k.cls = g.cls[((long long)q.b * g.n_qtiles + q.g) * g.n_ktiles + kg];
-    } else {
-        k.cls = g.causal ? causal_class(q, k) : BA_TILE_FULL;
-        // without a class map, masks force per-element predicates
-        if (k.cls == BA_TILE_FULL && (g.kpm || g.am)) k.cls = BA_TILE_PARTIAL;
+}
+
+// Moves to the next chunk of the walk; false when the walk is over.
+__host__ __device__ __forceinline__ bool kwalk_next_chunk(const Geom &g, KWalk &w) {
+    w.t = 0;
+    if (!g.ring) return false;
+    if (++w.ci < w.n_ch) {
+        w.c = 2 * g.P - 1 - w.src;
+        return true;
     }
-    return k;
+    w.ci = 0;
+    if (++w.s >= g.s_end) return false;
+    w.src = w.src == 0 ? g.P - 1 : w.src - 1;
+    w.c = w.src;
+    return true;
+}
+
+// Next non-EMPTY key tile of the walk into k; false at the end.
+__host__ __device__ __forceinline__ bool kwalk_next(const Geom &g, const QTile &q, KWalk &w, KTile &k) {
+    const long long q_last = q.pos0 + q.len - 1;
+    const int per_chunk = g.ring ? g.nkt_pc : g.n_ktiles;
+    const int chunk_len = g.ring ? g.CL : g.Lk;
+    for (;;) {
+        if (w.t >= per_chunk) {
+            if (!kwalk_next_chunk(g, w)) return false;
+            continue;
+        }
+        const int start = w.t * TILE;                      // within the chunk
+        k.idx = w.c * per_chunk + w.t;
+        k.row0 = (g.ring ? w.c * g.CL : 0) + start;
+        k.len = chunk_len - start < TILE ? chunk_len - start : TILE;
+        k.pos0 = g.ring ? (long long)k.row0 : g.k_off + k.row0;
+        ++w.t;
+        if (g.cls) {
+            k.cls = g.cls[((long long)q.b * g.n_qtiles + q.g) * g.n_ktiles + k.idx];
+            if (k.cls == BA_TILE_EMPTY) continue;
+            return true;
+        }
+        if (g.causal && k.pos0 > q_last) {                 // this and the rest of the chunk lie in the future
+            w.t = per_chunk;
+            continue;
+        }
+        k.cls = (!g.causal || k.pos0 + k.len - 1 <= q.pos0) ? BA_TILE_FULL : BA_TILE_PARTIAL;
+        if (k.cls == BA_TILE_FULL && (g.kpm || g.am)) k.cls = BA_TILE_PARTIAL;   // masks need predicates
+        return true;
+    }
 }
 
 // Work item w -> (q tile, b, h).  Items are grouped by heads_per_group (b, h)

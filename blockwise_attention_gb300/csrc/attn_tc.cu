@@ -34,32 +34,22 @@
 namespace ba {
 namespace {
 
-// PV of key tile j is issued after QK of tile j + PV_LAG.  With two S and two
-// P buffers in TMEM, a lag of 1 keeps one QK queued behind every PV (a lag of 2
-// measured no better on the 8K and 64K causal workloads).
-constexpr int PV_LAG = 1;
-
 template <int D>
 struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
     static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
-    static constexpr int KS = D == 128 ? 3 : 4;    // K stages
-    static constexpr int VS = D == 128 ? 3 : 4;    // V stages
+    static constexpr int NS = D == 128 ? 3 : 4;    // stages, each one K tile and one V tile
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
-    static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
+    static constexpr int KV_OFF = TILE_BYTES;      // stage i: K at KV_OFF + 2i*TILE_BYTES, V right after
+    static constexpr int BAR_OFF = KV_OFF + NS * 2 * TILE_BYTES;
     enum {
         B_QFULL = 0,
         B_QEMPTY,
-        B_KFULL,
-        B_KEMPTY = B_KFULL + KS,
-        B_VFULL = B_KEMPTY + KS,
-        B_VEMPTY = B_VFULL + VS,
-        B_SFULL = B_VEMPTY + VS,
-        B_SEMPTY = B_SFULL + 2,
-        B_PFULL = B_SEMPTY + 2,
+        B_KVFULL,
+        B_KVEMPTY = B_KVFULL + NS,
+        B_SFULL = B_KVEMPTY + NS,
+        B_PFULL = B_SFULL + 2,
         B_PVDONE = B_PFULL + 2,
         B_OFULL = B_PVDONE + 2,
         B_OEMPTY,
@@ -225,7 +215,7 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw_base);
-    const uint32_t sQ = base + C::Q_OFF, sK = base + C::K_OFF, sV = base + C::V_OFF;
+    const uint32_t sQ = base + C::Q_OFF, sKV = base + C::KV_OFF;
     const uint32_t bars = base + C::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
@@ -238,17 +228,12 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QEMPTY), 1);
-        for (int i = 0; i < C::KS; ++i) {
-            mbar_init(bar(C::B_KFULL + i), 1);
-            mbar_init(bar(C::B_KEMPTY + i), 1);
-        }
-        for (int i = 0; i < C::VS; ++i) {
-            mbar_init(bar(C::B_VFULL + i), 1);
-            mbar_init(bar(C::B_VEMPTY + i), 1);
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(bar(C::B_KVFULL + i), 1);
+            mbar_init(bar(C::B_KVEMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
-            mbar_init(bar(C::B_SEMPTY + i), 128);
             mbar_init(bar(C::B_PFULL + i), 128);
             mbar_init(bar(C::B_PVDONE + i), 1);
         }
@@ -279,7 +264,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t kfill = 0, vfill = 0, qfills = 0, it_local = 0;
+            uint32_t fill = 0, qfills = 0, it_local = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
                 const QTile qt = work_item(g, w);
@@ -295,27 +280,19 @@ __global__ void __launch_bounds__(256, 1)
                 kwalk_begin(g, qt, wk);
                 KTile kt;
                 while (kwalk_next(g, qt, wk, kt)) {
-                    uint32_t st = kfill % C::KS, use = kfill / C::KS;
-                    if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                    const uint32_t st = fill % C::NS, use = fill / C::NS;
+                    if (use > 0 && !mbar_wait(bar(C::B_KVEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
+                    const uint32_t dst = sKV + st * 2 * C::TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE_BYTES);
                     for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h,
-                                    qt.b, bar(C::B_KFULL + st));
-                    ++kfill;
-                    st = vfill % C::VS;
-                    use = vfill / C::VS;
-                    if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
+                        tma_load_4d(dst + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h, qt.b, bar(C::B_KVFULL + st));
                     for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt.row0, qt.h,
-                                    qt.b, bar(C::B_VFULL + st));
-                    ++vfill;
+                        tma_load_4d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt.row0, qt.h, qt.b,
+                                    bar(C::B_KVFULL + st));
+                    ++fill;
                 }
             }
             if (!ok) {
@@ -323,22 +300,26 @@ __global__ void __launch_bounds__(256, 1)
                 volatile int never = 0;
                 const uint64_t lim2 = 200000000ull;
                 if (qfills > 0) mbar_wait(bar(C::B_QFULL), (qfills - 1) & 1, &never, nullptr, lim2);
-                for (uint32_t i = 0; i < (uint32_t)C::KS && i < kfill; ++i) {
-                    const uint32_t last = kfill - 1 - i;
-                    mbar_wait(bar(C::B_KFULL + last % C::KS), (last / C::KS) & 1, &never, nullptr, lim2);
-                }
-                for (uint32_t i = 0; i < (uint32_t)C::VS && i < vfill; ++i) {
-                    const uint32_t last = vfill - 1 - i;
-                    mbar_wait(bar(C::B_VFULL + last % C::VS), (last / C::VS) & 1, &never, nullptr, lim2);
+                for (uint32_t i = 0; i < (uint32_t)C::NS && i < fill; ++i) {
+                    const uint32_t last = fill - 1 - i;
+                    mbar_wait(bar(C::B_KVFULL + last % C::NS), (last / C::NS) & 1, &never, nullptr, lim2);
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Per key tile j: wait K/V of j, QK(j) -> S[j % 2], then PV(j - 1) once the
+        // softmax has written P(j - 1).  QK(j + 1) is therefore issued only after
+        // P(j - 1) exists, which implies S(j - 1) was read: no separate "S free"
+        // barrier is needed.  The S_FULL(j) commit covers every earlier MMA, so the
+        // softmax may overwrite P(j % 2) (last read by PV(j - 2)) once S(j) is full.
         if (lane == 0) {
-            uint32_t kcons = 0, vcons = 0, scnt = 0, pcnt = 0, it_local = 0;
+            uint32_t cons = 0, scnt = 0, pcnt = 0, it_local = 0;
             bool ok = true;
+            const uint64_t qdesc0 = sdesc(sQ, 16, 1024);            // K-major, 128B swizzle
+            const uint64_t kdesc0 = sdesc(sKV, 16, 1024);
+            const uint64_t vdesc0 = sdesc(sKV + C::TILE_BYTES, C::BOX_BYTES, 1024);  // MN-major
             for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
                 const QTile qt = work_item(g, w);
                 if (!mbar_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
@@ -346,82 +327,71 @@ __global__ void __launch_bounds__(256, 1)
                     break;
                 }
                 tc_fence_after();
-                bool first_pv = true;
-                uint32_t pending = 0;   // tiles whose QK is issued but whose PV is not yet
                 // O of the previous item must have been read out before this item
-                // writes O or signals O_FULL.  Waited exactly once per item, so the
-                // O_FULL / O_EMPTY phases never run two ahead of their waiters (an
-                // item without key tiles issues no PV but still commits O_FULL).
+                // writes O or signals O_FULL: waited exactly once per item, so the
+                // O_FULL / O_EMPTY phases never run two ahead of their waiters.
                 bool o_free = it_local == 0;
-                auto wait_o_free = [&]() -> bool {
-                    if (o_free) return true;
-                    o_free = true;
-                    return mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim);
-                };
-                auto issue_pv = [&]() -> bool {
-                    const uint32_t vs = vcons % C::VS, pb = pcnt & 1;
-                    if (!mbar_wait(bar(C::B_VFULL + vs), (vcons / C::VS) & 1, abort, a.err, lim)) return false;
-                    if (!mbar_wait(bar(C::B_PFULL + pb), (pcnt >> 1) & 1, abort, a.err, lim)) return false;
-                    if (first_pv && !wait_o_free()) return false;
-                    tc_fence_after();
-                    const uint32_t vbase = sV + vs * C::TILE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < TILE / 16; ++kk) {
-                        uint64_t bd = sdesc(vbase + kk * 2048, C::BOX_BYTES, 1024);
-                        mma_ts(tmem + C::O_COL, tmem + C::P_COL + pb * 64 + kk * 8, bd, C::IDESC_PV,
-                               (first_pv && kk == 0) ? 0u : 1u);
-                    }
-                    mma_commit(bar(C::B_VEMPTY + vs));
-                    mma_commit(bar(C::B_PVDONE + pb));
-                    ++vcons;
-                    ++pcnt;
-                    --pending;
-                    first_pv = false;
-                    return true;
-                };
+                bool first_pv = true, have_prev = false;
+                uint32_t prev_st = 0;
                 KWalk wk;
                 kwalk_begin(g, qt, wk);
                 KTile kt;
-                while (ok && kwalk_next(g, qt, wk, kt)) {
-                    const uint32_t ks = kcons % C::KS, sb = scnt & 1;
-                    if (!mbar_wait(bar(C::B_KFULL + ks), (kcons / C::KS) & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    if (scnt >= 2 && !mbar_wait(bar(C::B_SEMPTY + sb), ((scnt >> 1) - 1) & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kbase = sK + ks * C::TILE_BYTES;
+                for (;;) {
+                    const bool more = kwalk_next(g, qt, wk, kt);
+                    uint32_t st = 0;
+                    if (more) {
+                        st = cons % C::NS;
+                        if (!mbar_wait(bar(C::B_KVFULL + st), (cons / C::NS) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t kd = kdesc0 + (uint64_t)((st * 2 * C::TILE_BYTES) >> 4);
+                        const uint32_t sd = tmem + C::S_COL + (scnt & 1) * 128;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                        mma_ss(tmem + C::S_COL + sb * 128, sdesc(sQ + off, 16, 1024), sdesc(kbase + off, 16, 1024),
-                               C::IDESC_QK, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                            mma_ss(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(C::B_SFULL + (scnt & 1)));
+                        ++cons;
+                        ++scnt;
+                    } else {
+                        mma_commit(bar(C::B_QEMPTY));   // every QK of the item is issued
                     }
-                    mma_commit(bar(C::B_SFULL + sb));
-                    mma_commit(bar(C::B_KEMPTY + ks));
-                    ++kcons;
-                    ++scnt;
-                    ++pending;
-                    // PV of tile j - PV_LAG follows QK of tile j, so the tensor pipe has
-                    // QK work queued while the softmax of the lagging tiles runs.
-                    if (pending > (uint32_t)PV_LAG && !issue_pv()) {
-                        ok = false;
-                        break;
+                    if (have_prev) {
+                        // PV of the previous tile
+                        const uint32_t pb = pcnt & 1;
+                        if (!mbar_wait(bar(C::B_PFULL + pb), (pcnt >> 1) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!o_free) {
+                            if (!mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
+                                ok = false;
+                                break;
+                            }
+                            o_free = true;
+                        }
+                        tc_fence_after();
+                        // descriptor start-address field advances by bytes / 16
+                        const uint64_t vd = vdesc0 + (uint64_t)((prev_st * 2 * C::TILE_BYTES) >> 4);
+                        const uint32_t pa = tmem + C::P_COL + pb * 64;
+#pragma unroll
+                        for (int kk = 0; kk < TILE / 16; ++kk)
+                            mma_ts(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
+                                   (first_pv && kk == 0) ? 0u : 1u);
+                        mma_commit(bar(C::B_KVEMPTY + prev_st));
+                        mma_commit(bar(C::B_PVDONE + pb));
+                        ++pcnt;
+                        first_pv = false;
                     }
+                    have_prev = more;
+                    prev_st = st;
+                    if (!more) break;
                 }
                 if (!ok) break;
-                mma_commit(bar(C::B_QEMPTY));
-                while (pending > 0) {
-                    if (!issue_pv()) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!ok) break;
-                if (!wait_o_free()) {
+                if (!o_free && !mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
@@ -468,8 +438,6 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int j = 0; j < TILE; ++j) s[j] = __uint_as_float(r[j]);
                 }
-                tc_fence_before();
-                mbar_arrive(bar(C::B_SEMPTY + sb));
 
                 if (kt.cls == BA_TILE_PARTIAL || kt.len < TILE) {
                     const bool row_valid = row < qt.len;   // rows past the tile end are never stored
@@ -506,12 +474,7 @@ __global__ void __launch_bounds__(256, 1)
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;
 
-                const uint32_t pb = scnt & 1;
-                if (scnt >= 2 && !warp_wait(bar(C::B_PVDONE + pb), ((scnt >> 1) - 1) & 1, abort, a.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                const uint32_t pb = scnt & 1;   // last read by PV(j - 2), complete once S(j) is full
 #pragma unroll
                 for (int c = 0; c < TILE / 64; ++c)
                     tmem_st32(tmem + lane_addr + C::P_COL + pb * 64 + c * 32,

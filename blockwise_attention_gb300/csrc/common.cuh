@@ -136,72 +136,95 @@ __host__ __device__ inline int causal_class(const QTile &q, const KTile &k) {
 // agree on the sequence without communicating.  Without a class map, causal
 // EMPTY tiles are skipped chunk-wise (a key tile, and every later tile of its
 // chunk, is EMPTY once its first key lies after the query tile's last row).
+// The state is kept in 32-bit integers and advanced by additions: the walk
+// runs on the single MMA-issuing thread, where its latency is on the critical
+// path of every tile.
 struct KWalk {
-    int s;       // ring step (ring mode)
-    int ci;      // chunk of the source rank, in its local order (ring mode)
-    int t;       // tile within the chunk
-    int c;       // global chunk id
-    int n_ch;    // chunks per rank
-    int src;     // source rank of step s
+    int row;        // first k/v row of the next tile
+    int chunk_end;  // end row of the current chunk
+    int idx;        // tile id of the next tile (class-map column)
+    int s, ci, src; // ring step, chunk of the source rank, source rank
+    int q_last;     // global position of the query tile's last row
+    int q_first;    // global position of the query tile's first row
+    int pos_off;    // global position = row + pos_off
 };
 
+__host__ __device__ __forceinline__ void kwalk_set_chunk(const Geom &g, KWalk &w, int c) {
+    w.row = c * g.CL;
+    w.chunk_end = w.row + g.CL;
+    w.idx = c * g.nkt_pc;
+}
+
 __host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile &q, KWalk &w) {
-    w.t = 0;
+    w.q_first = (int)q.pos0;
+    w.q_last = (int)q.pos0 + q.len - 1;
     w.ci = 0;
     if (g.ring) {
+        w.pos_off = 0;
         w.s = g.s_begin;
-        w.n_ch = g.zigzag ? 2 : 1;
         w.src = ((q.rank - w.s) % g.P + g.P) % g.P;
-        w.c = w.src;
+        if (w.s < g.s_end) {
+            kwalk_set_chunk(g, w, w.src);
+        } else {
+            w.row = w.chunk_end = 0;   // empty step range: the walk is over
+            w.ci = 1;
+            w.s = g.s_end;
+        }
     } else {
+        w.pos_off = (int)g.k_off;
         w.s = 0;
-        w.n_ch = 1;
         w.src = 0;
-        w.c = 0;
+        w.row = 0;
+        w.chunk_end = g.Lk;
+        w.idx = 0;
     }
 }
 
 // Moves to the next chunk of the walk; false when the walk is over.
 __host__ __device__ __forceinline__ bool kwalk_next_chunk(const Geom &g, KWalk &w) {
-    w.t = 0;
     if (!g.ring) return false;
-    if (++w.ci < w.n_ch) {
-        w.c = 2 * g.P - 1 - w.src;
+    if (g.zigzag && w.ci == 0) {
+        w.ci = 1;
+        kwalk_set_chunk(g, w, 2 * g.P - 1 - w.src);
         return true;
     }
     w.ci = 0;
     if (++w.s >= g.s_end) return false;
     w.src = w.src == 0 ? g.P - 1 : w.src - 1;
-    w.c = w.src;
+    kwalk_set_chunk(g, w, w.src);
     return true;
 }
 
 // Next non-EMPTY key tile of the walk into k; false at the end.
 __host__ __device__ __forceinline__ bool kwalk_next(const Geom &g, const QTile &q, KWalk &w, KTile &k) {
-    const long long q_last = q.pos0 + q.len - 1;
-    const int per_chunk = g.ring ? g.nkt_pc : g.n_ktiles;
-    const int chunk_len = g.ring ? g.CL : g.Lk;
     for (;;) {
-        if (w.t >= per_chunk) {
+        if (w.row >= w.chunk_end) {
             if (!kwalk_next_chunk(g, w)) return false;
             continue;
         }
-        const int start = w.t * TILE;                      // within the chunk
-        k.idx = w.c * per_chunk + w.t;
-        k.row0 = (g.ring ? w.c * g.CL : 0) + start;
-        k.len = chunk_len - start < TILE ? chunk_len - start : TILE;
-        k.pos0 = g.ring ? (long long)k.row0 : g.k_off + k.row0;
-        ++w.t;
+        const int row = w.row;
+        const int pos = row + w.pos_off;
+        const int rem = w.chunk_end - row;
+        k.row0 = row;
+        k.len = rem < TILE ? rem : TILE;
+        k.pos0 = pos;
+        k.idx = w.idx;
+        w.row = row + TILE;
+        ++w.idx;
         if (g.cls) {
             k.cls = g.cls[((long long)q.b * g.n_qtiles + q.g) * g.n_ktiles + k.idx];
             if (k.cls == BA_TILE_EMPTY) continue;
             return true;
         }
-        if (g.causal && k.pos0 > q_last) {                 // this and the rest of the chunk lie in the future
-            w.t = per_chunk;
-            continue;
+        if (g.causal) {
+            if (pos > w.q_last) {          // this and the rest of the chunk lie in the future
+                w.row = w.chunk_end;
+                continue;
+            }
+            k.cls = pos + k.len - 1 <= w.q_first ? BA_TILE_FULL : BA_TILE_PARTIAL;
+        } else {
+            k.cls = BA_TILE_FULL;
         }
-        k.cls = (!g.causal || k.pos0 + k.len - 1 <= q.pos0) ? BA_TILE_FULL : BA_TILE_PARTIAL;
         if (k.cls == BA_TILE_FULL && (g.kpm || g.am)) k.cls = BA_TILE_PARTIAL;   // masks need predicates
         return true;
     }

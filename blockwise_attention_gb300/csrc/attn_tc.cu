@@ -56,7 +56,7 @@ struct Cfg {
         B_DRAIN,
         NBAR
     };
-    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort flag
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort flag, [2] item tiles
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t S_COL = 0;
     static constexpr uint32_t P_COL = 256;
@@ -272,6 +272,17 @@ __global__ void __launch_bounds__(256, 1)
                     ok = false;
                     break;
                 }
+                {
+                    // Number of key tiles of this item, for the MMA thread (published by
+                    // the Q_FULL arrive below; the MMA thread reads it after Q_FULL and
+                    // the next write happens after Q_EMPTY, i.e. after all its QKs).
+                    KWalk cw;
+                    kwalk_begin(g, qt, cw);
+                    KTile ct;
+                    uint32_t n = 0;
+                    while (kwalk_next(g, qt, cw, ct)) ++n;
+                    misc[2] = n;
+                }
                 mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
                 for (int bx = 0; bx < C::NBOX; ++bx)
                     tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, qt.row0, qt.h, qt.b, bar(C::B_QFULL));
@@ -321,7 +332,6 @@ __global__ void __launch_bounds__(256, 1)
             const uint64_t kdesc0 = sdesc(sKV, 16, 1024);
             const uint64_t vdesc0 = sdesc(sKV + C::TILE_BYTES, C::BOX_BYTES, 1024);  // MN-major
             for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
-                const QTile qt = work_item(g, w);
                 if (!mbar_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
@@ -333,19 +343,18 @@ __global__ void __launch_bounds__(256, 1)
                 bool o_free = it_local == 0;
                 bool first_pv = true, have_prev = false;
                 uint32_t prev_st = 0;
-                KWalk wk;
-                kwalk_begin(g, qt, wk);
-                KTile kt;
-                for (;;) {
-                    const bool more = kwalk_next(g, qt, wk, kt);
+                const uint32_t n_tiles = misc[2];
+                for (uint32_t t = 0;; ++t) {
+                    const bool more = t < n_tiles;
                     uint32_t st = 0;
                     if (more) {
                         st = cons % C::NS;
+                        // TMA data is ordered by the barrier itself; S[scnt & 1] was last
+                        // read by the softmax of tile j - 2, ordered by P_FULL(j - 2) below.
                         if (!mbar_wait(bar(C::B_KVFULL + st), (cons / C::NS) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
                         const uint64_t kd = kdesc0 + (uint64_t)((st * 2 * C::TILE_BYTES) >> 4);
                         const uint32_t sd = tmem + C::S_COL + (scnt & 1) * 128;
 #pragma unroll

@@ -73,6 +73,39 @@ def visible_pairs(w, inp) -> int:
     return total * w.H
 
 
+KERNEL_SOURCES = ["blockwise_attention_gb300/csrc/attn_tc.cu", "blockwise_attention_gb300/csrc/common.cuh",
+                  "blockwise_attention_gb300/csrc/epilogue.cuh", "blockwise_attention_gb300/csrc/internal.h"]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes of one attention launch from the committed ncu summary of this
+    workload, or None when the kernel sources changed since it was captured."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", f"attn_tc_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    t = re.search(r"^traffic_bytes:\s*(\d+)", text, re.M)
+    h = re.search(r"^source_sha256:\s*([0-9a-f]+)", text, re.M)
+    if not t or not h:
+        return None
+    sha = hashlib.sha256()
+    for src in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            sha.update(f.read())
+    return int(t.group(1)) if sha.hexdigest() == h.group(1) else None
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -272,10 +305,7 @@ def native_arm(args, w, rank, world, local_rank):
     total_ms = t_start.elapsed_time(t_end)
     attn_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
     rope_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
     kernels_per_step = (1 if rope else 0) + (1 if args.mode == "fused" else w.P) + \
@@ -316,10 +346,7 @@ def native_arm(args, w, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         e_ms = a.elapsed_time(b) / args.steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, dev)
         h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
         d2h = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -336,7 +363,7 @@ def native_arm(args, w, rank, world, local_rank):
     achieved = flops / (attn_avg * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": None, "kernel": "attn_tc_kernel<128>",
+            "traffic": profiled_traffic(w.name), "kernel": f"attn_tc_kernel<{w.d}>",
             "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a repeated step)",
             "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"]),
             "kernel_ms": attn_avg}

@@ -117,6 +117,11 @@ def attention(q, k, v, *, causal=False, kpm=None, am=None, scale=None, q_pos0=0,
     S = k.shape[2]
     assert k.shape == (B, H, S, d) and v.shape == (B, H, S, d)
     kpm, am = _u8(kpm), _u8(am)
+    # masks are indexed at global positions: they must cover every position used
+    if kpm is not None and (kpm.shape[0] < B or kpm.shape[1] < k_pos0 + S):
+        raise ValueError("key_padding_mask does not cover the key positions")
+    if am is not None and (am.shape[0] < q_pos0 + L or am.shape[1] < k_pos0 + S):
+        raise ValueError("attn_mask does not cover the (query, key) positions")
     if rows is not None:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         n = rows.size

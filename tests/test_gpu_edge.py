@@ -37,6 +37,26 @@ def test_block_ragged_offsets(dt, d, causal):
     compare(out, lse, o_ref, l_ref, dt, f"block {dt} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("bf16", 64), ("f32", 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_masks_at_offsets(dt, d, causal):
+    """attn_block_fwd with key padding and attn_mask indexed at global positions."""
+    B, H, Lq, Lk, q_off, k_off = 2, 3, 260, 300, 140, 100
+    q, k, v = rand((B, H, Lq, d), DT[dt], 60), rand((B, H, Lk, d), DT[dt], 61), rand((B, H, Lk, d), DT[dt], 62)
+    rng = np.random.default_rng(1)
+    kpm = (rng.random((B, k_off + Lk)) < 0.2).astype(np.uint8)
+    am = (rng.random((q_off + Lq, k_off + Lk)) < 0.3).astype(np.uint8)
+    am[q_off + 9, :] = 1                   # local row 9 sees nothing
+    am[:, k_off + 128:k_off + 256] = 1     # an EMPTY key tile
+    kpm_t, am_t = torch.from_numpy(kpm).cuda(), torch.from_numpy(am).cuda()
+    out, lse = ba.attn_block_fwd(q, k, v, q_off=q_off, k_off=k_off, key_padding_mask=kpm_t, attn_mask=am_t,
+                                 causal=causal, out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=causal, kpm=kpm,
+                                    am=am, q_pos0=q_off, k_pos0=k_off)
+    compare(out, lse, o_ref, l_ref, dt, f"block masks {dt} d={d} causal={causal}")
+    assert torch.all(lse[:, :, 9] == -math.inf)
+
+
 @pytest.mark.parametrize("T,P,part", [(1000, 4, "zigzag"), (1000, 4, "contiguous"), (384, 3, "zigzag"),
                                       (640, 1, "contiguous"), (96, 2, "zigzag")])
 @pytest.mark.parametrize("mode", ["fused", "stepwise"])

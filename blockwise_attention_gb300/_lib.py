@@ -26,6 +26,8 @@ ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 BA_OK, BA_ERR_ARG, BA_ERR_SHAPE, BA_ERR_CUDA, BA_ERR_TIMEOUT, BA_ERR_UNSUPPORTED, BA_ERR_WORKSPACE = \
     0, -1, -2, -3, -4, -5, -6
+BA_ERR_NOALLOC_LIMIT = -7
+BA_NOALLOC_MAX_CLASS_BYTES = 1 << 20
 BA_F32, BA_BF16 = 0, 1
 PARTITIONS = {"contiguous": 0, "zigzag": 1}
 MODES = {"stepwise": 0, "fused": 1}
@@ -93,7 +95,7 @@ class ba_tensor(ctypes.Structure):
 
 EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ring_attn_fwd",
             "ring_attn_fwd_workspace_size", "rope_apply", "ba_tile_classes", "ba_index_maps",
-            "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror"]
+            "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc"]
 
 
 def load(path: str | None = None):
@@ -113,6 +115,9 @@ def load(path: str | None = None):
     lib.attn_block_fwd.restype = i
     lib.attn_block_fwd.argtypes = [T, T, T, i, i, i, i, i, i, i64, i64, vp, i64, vp, i64, i, f, vp, i, vp, i,
                                    vp, sz, vp]
+    lib.attn_block_fwd_noalloc.restype = i
+    lib.attn_block_fwd_noalloc.argtypes = [T, T, T, i, i, i, i, i, i, i64, i64, vp, i64, vp, i64, i, f, vp, i, vp,
+                                           i, vp]
     lib.attn_merge.restype = i
     lib.attn_merge.argtypes = [vp, vp, vp, vp, i64, i, vp]
     lib.ring_attn_fwd_workspace_size.restype = sz
@@ -197,6 +202,24 @@ def attn_block_fwd(q, k, v, *, q_off=0, k_off=0, key_padding_mask=None, attn_mas
                             _ptr(out), _dtype_code(out.dtype), _ptr(lse), int(bool(accumulate)),
                             _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
     _check("attn_block_fwd", rc)
+    return out, lse
+
+
+def attn_block_fwd_noalloc(q, k, v, out, lse, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None,
+                           causal=False, scale=None, accumulate=False, stream=None):
+    """attn_block_fwd for callers that cannot allocate device memory: the caller
+    passes out and lse, and the library allocates nothing (its tile-class scratch
+    is a fixed device array of BA_NOALLOC_MAX_CLASS_BYTES).  Returns (out, lse)."""
+    lib = load()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    rc = lib.attn_block_fwd_noalloc(_tensor(q), _tensor(k), _tensor(v), B, H, Lq, Lk, d, _dtype_code(q.dtype),
+                                    q_off, k_off, kpm, kpm_ld, am, am_ld, int(bool(causal)),
+                                    0.0 if scale is None else float(scale), _ptr(out), _dtype_code(out.dtype),
+                                    _ptr(lse), int(bool(accumulate)), _stream(stream))
+    _check("attn_block_fwd_noalloc", rc)
     return out, lse
 
 

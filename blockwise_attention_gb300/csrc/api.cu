@@ -21,6 +21,10 @@ namespace {
 // ---------------------------------------------------------------------------
 __device__ unsigned g_err_word;
 
+// Fixed scratch of attn_block_fwd_noalloc: the tile-class map, for callers that
+// cannot allocate.  Present on every device that loads the library.
+static __device__ __align__(256) int8_t g_noalloc_classes[BA_NOALLOC_MAX_CLASS_BYTES];
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned *g_err_ptr[kMaxDevices];
@@ -44,6 +48,22 @@ int device_setup(int dev) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BA_ERR_CUDA;
     g_num_sms[dev] = sms;
     g_err_ptr[dev] = static_cast<unsigned *>(p);
+    return BA_OK;
+}
+
+// Device address of g_noalloc_classes on device `dev` (which must be current),
+// looked up on the first call on that device.  Host code may not use the
+// array's name as a device pointer: it names a host-side stand-in.
+int8_t *g_noalloc_ptr[kMaxDevices];
+
+int noalloc_scratch(int dev, int8_t **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_classes) != cudaSuccess || p == nullptr) return BA_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int8_t *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
     return BA_OK;
 }
 
@@ -494,6 +514,7 @@ const char *ba_strerror(int code) {
         case BA_ERR_TIMEOUT: return "device wait timed out";
         case BA_ERR_UNSUPPORTED: return "unsupported combination";
         case BA_ERR_WORKSPACE: return "workspace too small";
+        case BA_ERR_NOALLOC_LIMIT: return "tile-class map larger than the fixed no-allocation scratch";
         default: return "unknown error";
     }
 }
@@ -808,6 +829,80 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
         if ((rc = run_attention(a, dev, T, T, stream))) return rc;
     }
     return BA_OK;
+}
+
+// Same work as attn_block_fwd, with the tile-class map in the library's fixed
+// device array instead of a workspace: nothing is allocated.
+int attn_block_fwd_noalloc(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,
+                           int64_t q_off, int64_t k_off, const uint8_t *key_padding_mask, int64_t kpm_ld,
+                           const uint8_t *attn_mask, int64_t am_ld, int causal, float scale, void *out,
+                           int out_dtype, float *lse, int accumulate, ba_stream_t stream) {
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || q_off < 0 || k_off < 0 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    const bool rows_exist = (long long)B * H * Lq > 0;
+    if (rows_exist && (check_tensor(q) || !out || !lse)) return BA_ERR_ARG;
+    if (rows_exist && Lk > 0 && (check_tensor(k) || check_tensor(v))) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
+    if (accumulate && out_dtype != BA_F32) return BA_ERR_ARG;
+    if ((key_padding_mask && kpm_ld < k_off + Lk) || (attn_mask && am_ld < k_off + Lk)) return BA_ERR_ARG;
+    const bool masks = key_padding_mask || attn_mask;
+    const size_t class_bytes = (size_t)B * ceil_div(Lq, TILE) * ceil_div(Lk, TILE);
+    if (masks && class_bytes > (size_t)BA_NOALLOC_MAX_CLASS_BYTES) return BA_ERR_NOALLOC_LIMIT;
+    if (B == 0 || H == 0 || Lq == 0) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    int8_t *classes = nullptr;
+    if (masks && (rc = noalloc_scratch(dev, &classes))) return rc;
+    const bool tc = tc_supported(dtype, d) && Lk > 0;
+    q = fix_unit_strides(q, B, H, Lq, d);
+    k = fix_unit_strides(k, B, H, Lk, d);
+    v = fix_unit_strides(v, B, H, Lk, d);
+    if (tc && (!tma_ok(q, B, H) || !tma_ok(k, B, H) || !tma_ok(v, B, H))) return BA_ERR_ARG;
+
+    AttnArgs a;
+    std::memset(&a, 0, sizeof a);
+    Geom &g = a.g;
+    g.B = B;
+    g.H = H;
+    g.d = d;
+    g.Lq = Lq;
+    g.Lk = Lk;
+    g.q_off = q_off;
+    g.k_off = k_off;
+    g.nqt_pc = g.n_qtiles = ceil_div(Lq, TILE);
+    g.nkt_pc = g.n_ktiles = ceil_div(Lk, TILE);
+    g.heads_per_group = heads_per_group(B, H, Lk, d, dtype);
+    g.n_items = g.n_qtiles * B * H;
+    g.causal = causal != 0;
+    g.kpm = key_padding_mask;
+    g.kpm_ld = kpm_ld;
+    g.am = attn_mask;
+    g.am_ld = am_ld;
+    if (masks) {
+        // every entry the attention kernel reads is written here first
+        g.cls = classes;
+        if ((rc = run_tile_classes(g, classes, stream))) return rc;
+    }
+    a.q = q.ptr;
+    a.k = k.ptr;
+    a.v = v.ptr;
+    a.qsB = q.sB; a.qsH = q.sH; a.qsT = q.sT;
+    a.ksB = k.sB; a.ksH = k.sH; a.ksT = k.sT;
+    a.vsB = v.sB; a.vsH = v.sH; a.vsT = v.sT;
+    a.dtype = dtype;
+    const float sc = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.scale_log2 = sc * LOG2E;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse;
+    a.rows = Lq;
+    a.acc_o = accumulate ? static_cast<const float *>(out) : nullptr;
+    a.acc_lse = accumulate ? lse : nullptr;
+    a.err = g_err_ptr[dev];
+    a.wait_limit_ns = kWaitLimitNs;
+    return run_attention(a, dev, Lq, Lk, stream);
 }
 
 }  // extern "C"

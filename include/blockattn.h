@@ -54,7 +54,8 @@ enum {
     BA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
     BA_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired */
     BA_ERR_UNSUPPORTED = -5, /* combination not implemented */
-    BA_ERR_WORKSPACE = -6    /* workspace smaller than required */
+    BA_ERR_WORKSPACE = -6,   /* workspace smaller than required */
+    BA_ERR_NOALLOC_LIMIT = -7 /* larger than the fixed scratch of attn_block_fwd_noalloc */
 };
 
 enum { BA_F32 = 0, BA_BF16 = 1 };
@@ -190,6 +191,40 @@ int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off,
  * order as ring_attn_fwd.  Returns BA_ERR_SHAPE for indivisible T.
  */
 int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule);
+
+/*
+ * attn_block_fwd_noalloc -- attn_block_fwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart; this is a library-level
+ * variant.  Some hosts own every device allocation themselves (for example a
+ * framework that plans all buffers ahead of execution and forbids allocation
+ * while it runs, or a process that works under a hard memory budget), so they
+ * can neither pass a workspace nor let the library call cudaMalloc.  This
+ * entry point takes the same arguments as attn_block_fwd minus the workspace
+ * and performs no allocation of any kind: the one piece of scratch
+ * attn_block_fwd needs -- the tile-class map built when a key-padding mask or
+ * attn_mask is given, B * ceil(Lq/128) * ceil(Lk/128) bytes -- lives in a
+ * fixed device array of BA_NOALLOC_MAX_CLASS_BYTES bytes inside the library,
+ * present on every GPU that loads the library until the process exits.
+ *  - Inputs and outputs are the caller's, exactly as for attn_block_fwd.
+ *  - A call whose tile-class map would exceed BA_NOALLOC_MAX_CLASS_BYTES
+ *    returns BA_ERR_NOALLOC_LIMIT before launching anything.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - All calls on a GPU share that GPU's array, and it keeps the last call's
+ *    contents.  Every entry a call reads is first written by that call, so
+ *    nothing needs clearing; but calls that overlap on the same GPU (for
+ *    example on two streams) race on it when they use masks: serialise them.
+ */
+#define BA_NOALLOC_MAX_CLASS_BYTES (1 << 20)
+int attn_block_fwd_noalloc(ba_tensor q, ba_tensor k, ba_tensor v,
+                           int B, int H, int Lq, int Lk, int d, int dtype,
+                           int64_t q_off, int64_t k_off,
+                           const uint8_t *key_padding_mask, int64_t kpm_ld,
+                           const uint8_t *attn_mask, int64_t am_ld,
+                           int causal, float scale,
+                           void *out, int out_dtype, float *lse, int accumulate,
+                           ba_stream_t stream);
 
 /* Synchronise `stream` and report whether any kernel launched by this library
  * on the current device since the previous call gave up a bounded device wait

@@ -56,7 +56,7 @@ struct Cfg {
         B_DRAIN,
         NBAR
     };
-    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort flag, [2] item tiles
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort, [2..3] item tiles
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t S_COL = 0;
     static constexpr uint32_t P_COL = 256;
@@ -268,20 +268,17 @@ __global__ void __launch_bounds__(256, 1)
             bool ok = true;
             for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
                 const QTile qt = work_item(g, w);
+                {
+                    // Number of key tiles of this item, for the MMA thread, counted while
+                    // the previous item still runs.  Slots alternate by item parity: slot it&1 was last read by
+                    // the MMA thread at the start of item it-2, before it committed
+                    // Q_EMPTY(it-2), which this thread waited for before loading Q(it-1).
+                    // Published by the Q_FULL arrive below.
+                    misc[2 + (it_local & 1)] = (uint32_t)kwalk_count(g, qt);
+                }
                 if (it_local > 0 && !mbar_wait(bar(C::B_QEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
-                }
-                {
-                    // Number of key tiles of this item, for the MMA thread (published by
-                    // the Q_FULL arrive below; the MMA thread reads it after Q_FULL and
-                    // the next write happens after Q_EMPTY, i.e. after all its QKs).
-                    KWalk cw;
-                    kwalk_begin(g, qt, cw);
-                    KTile ct;
-                    uint32_t n = 0;
-                    while (kwalk_next(g, qt, cw, ct)) ++n;
-                    misc[2] = n;
                 }
                 mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
                 for (int bx = 0; bx < C::NBOX; ++bx)
@@ -343,7 +340,7 @@ __global__ void __launch_bounds__(256, 1)
                 bool o_free = it_local == 0;
                 bool first_pv = true, have_prev = false;
                 uint32_t prev_st = 0;
-                const uint32_t n_tiles = misc[2];
+                const uint32_t n_tiles = misc[2 + (it_local & 1)];
                 for (uint32_t t = 0;; ++t) {
                     const bool more = t < n_tiles;
                     uint32_t st = 0;

@@ -230,6 +230,38 @@ __host__ __device__ __forceinline__ bool kwalk_next(const Geom &g, const QTile &
     }
 }
 
+// Number of key tiles kwalk_next yields for query tile q.  Without a class map
+// this is a sum over the walk's chunks (a chunk contributes its tiles that start
+// at or before q's last row under causal masking, all of them otherwise), so it
+// costs a few operations per chunk instead of a walk over every tile.
+__host__ __device__ inline int kwalk_count(const Geom &g, const QTile &q) {
+    if (g.cls) {
+        KWalk w;
+        kwalk_begin(g, q, w);
+        KTile k;
+        int n = 0;
+        while (kwalk_next(g, q, w, k)) ++n;
+        return n;
+    }
+    const long long q_last = q.pos0 + q.len - 1;
+    auto chunk_tiles = [&](long long first_pos, int len) -> int {
+        const int tiles = (len + TILE - 1) / TILE;
+        if (!g.causal) return tiles;
+        if (first_pos > q_last) return 0;
+        const long long upto = (q_last - first_pos) / TILE + 1;   // tiles starting at or before q_last
+        return upto < tiles ? (int)upto : tiles;
+    };
+    if (!g.ring) return chunk_tiles(g.k_off, g.Lk);
+    int n = 0;
+    int src = ((q.rank - g.s_begin) % g.P + g.P) % g.P;
+    for (int s = g.s_begin; s < g.s_end; ++s) {
+        n += chunk_tiles((long long)src * g.CL, g.CL);
+        if (g.zigzag) n += chunk_tiles((long long)(2 * g.P - 1 - src) * g.CL, g.CL);
+        src = src == 0 ? g.P - 1 : src - 1;
+    }
+    return n;
+}
+
 // Work item w -> (q tile, b, h).  Items are grouped by heads_per_group (b, h)
 // pairs so that concurrently running CTAs share K/V in L2; within a group the
 // query tiles come heaviest first under causal masking (latest positions).

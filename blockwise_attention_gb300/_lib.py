@@ -178,6 +178,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _check_out(out, lse, shape):
+    """Outputs are written as contiguous (B, H, L, d) and (B, H, L) buffers."""
+    if tuple(out.shape) != tuple(shape) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError(f"out must be a contiguous CUDA tensor of shape {tuple(shape)}")
+    if tuple(lse.shape) != tuple(shape[:3]) or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError(f"lse must be a contiguous float32 CUDA tensor of shape {tuple(shape[:3])}")
+
+
 def attn_block_fwd(q, k, v, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None, causal=False,
                    scale=None, out=None, out_dtype=None, lse=None, accumulate=False, workspace=None,
                    stream=None):
@@ -192,6 +200,7 @@ def attn_block_fwd(q, k, v, *, q_off=0, k_off=0, key_padding_mask=None, attn_mas
         out = torch.empty((B, H, Lq, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    _check_out(out, lse, (B, H, Lq, d))
     kpm, kpm_ld = _mask(key_padding_mask)
     am, am_ld = _mask(attn_mask)
     need = lib.attn_block_fwd_workspace_size(B, Lq, Lk, int(kpm is not None or am is not None))
@@ -213,6 +222,7 @@ def attn_block_fwd_noalloc(q, k, v, out, lse, *, q_off=0, k_off=0, key_padding_m
     lib = load()
     B, H, Lq, d = q.shape
     Lk = k.shape[2]
+    _check_out(out, lse, (B, H, Lq, d))
     kpm, kpm_ld = _mask(key_padding_mask)
     am, am_ld = _mask(attn_mask)
     rc = lib.attn_block_fwd_noalloc(_tensor(q), _tensor(k), _tensor(v), B, H, Lq, Lk, d, _dtype_code(q.dtype),
@@ -261,6 +271,7 @@ def ring_attn_fwd(q, k, v, *, P, partition="contiguous", mode="fused", key_paddi
         out = torch.empty((B, H, T, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    _check_out(out, lse, (B, H, T, d))
     kpm, kpm_ld = _mask(key_padding_mask)
     am, am_ld = _mask(attn_mask)
     masks = kpm is not None or am is not None

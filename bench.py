@@ -324,25 +324,58 @@ def native_arm(args, w, rank, world, local_rank):
                                                inp.kpm is not None or inp.am is not None, rope)
         wse = torch.empty(max(ws_e, 1), dtype=torch.uint8, device=dev)
 
+        # Independent groups of heads (B == 1) or batch items are pipelined over three
+        # streams: host->device copy of group g+1 and device->host copy of group g-1
+        # run while group g computes, each group one ring_attn_fwd call.
+        n_groups = 4
+        if w.B == 1 and w.H % n_groups == 0:
+            sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
+        elif w.B % n_groups == 0:
+            sl = [(slice(i * w.B // n_groups, (i + 1) * w.B // n_groups),) for i in range(n_groups)]
+        else:
+            n_groups, sl = 1, [(slice(None),)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(n_groups)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_groups)]
+        ev_out = [torch.cuda.Event() for _ in range(n_groups)]
+        started = [False]
+
         def e2e_step():
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            ba.ring_attn_fwd(qd, kd, vd, P=w.P, partition=w.partition, mode=args.mode,
-                             key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, rope=rope,
-                             rope_base=w.rope_base or 10000.0, out=out, lse=lse, workspace=wse)
-            oh.copy_(out, non_blocking=True)
-            lh.copy_(lse, non_blocking=True)
+            for i, ix in enumerate(sl):
+                kpm_i = inp.kpm[ix[0]] if inp.kpm is not None else None
+                with torch.cuda.stream(s_in):
+                    if started[0]:
+                        s_in.wait_event(ev_comp[i])      # previous step's compute read these inputs
+                    qd[ix].copy_(qh[ix], non_blocking=True)
+                    kd[ix].copy_(kh[ix], non_blocking=True)
+                    vd[ix].copy_(vh[ix], non_blocking=True)
+                    ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                if started[0]:
+                    stream.wait_event(ev_out[i])         # previous step's copy-out read these outputs
+                ba.ring_attn_fwd(qd[ix], kd[ix], vd[ix], P=w.P, partition=w.partition, mode=args.mode,
+                                 key_padding_mask=kpm_i, attn_mask=inp.am, causal=w.causal, rope=rope,
+                                 rope_base=w.rope_base or 10000.0, out=out[ix], lse=lse[ix], workspace=wse,
+                                 stream=stream)
+                ev_comp[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[i])
+                    oh[ix].copy_(out[ix], non_blocking=True)
+                    lh[ix].copy_(lse[ix], non_blocking=True)
+                    ev_out[i].record(s_out)
+            started[0] = True
 
         for _ in range(args.warmup):
             e2e_step()
         torch.cuda.synchronize()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        a.record(s_in)            # the first operation of a step is a copy on s_in
         for _ in range(args.steps):
             e2e_step()
-        b.record(stream)
+        stream.wait_event(ev_out[-1])
+        s_out.wait_stream(stream)
+        b.record(s_out)           # the last copy-out of the last step
         torch.cuda.synchronize()
         barrier()
         e_ms = a.elapsed_time(b) / args.steps
@@ -350,7 +383,7 @@ def native_arm(args, w, rank, world, local_rank):
         h2d = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
         d2h = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "pipeline_groups": n_groups}
         del qh, kh, vh, qd, kd, vd, wse
 
     if ba.sync_status() != 0:

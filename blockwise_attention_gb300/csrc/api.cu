@@ -86,6 +86,14 @@ size_t elem_size(int dtype) { return dtype == BA_F32 ? 4 : 2; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace block at the front of every attention workspace: one 32-bit item
+// counter per kernel launch of the call, zeroed on the stream before them.
+size_t sched_bytes(int launches) { return align256((size_t)4 * (size_t)(launches > 0 ? launches : 1)); }
+
+int zero_sched(void *p, int launches, cudaStream_t s) {
+    return cudaMemsetAsync(p, 0, (size_t)4 * (size_t)launches, s) == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
 bool valid_dtype(int t) { return t == BA_F32 || t == BA_BF16; }
 bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
@@ -421,6 +429,7 @@ struct Scratch {
         s = stream;
         if (need == 0) return BA_OK;
         if (ws) {
+            if (reinterpret_cast<uintptr_t>(ws) & 255) return BA_ERR_ARG;
             if (ws_bytes < need) return BA_ERR_WORKSPACE;
             ptr = ws;
             return BA_OK;
@@ -629,8 +638,10 @@ int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off, const u
 }
 
 size_t attn_block_fwd_workspace_size(int B, int Lq, int Lk, int has_masks) {
-    if (!has_masks) return 0;
-    return align256((size_t)B * ceil_div(Lq, TILE) * ceil_div(Lk, TILE));
+    if (B < 0 || Lq < 0 || Lk < 0) return 0;
+    size_t bytes = sched_bytes(1);
+    if (has_masks) bytes += align256((size_t)B * ceil_div(Lq, TILE) * ceil_div(Lk, TILE));
+    return bytes;
 }
 
 int attn_block_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,
@@ -680,9 +691,13 @@ int attn_block_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, 
     Scratch ws;
     if ((rc = ws.acquire(workspace, workspace_bytes, attn_block_fwd_workspace_size(B, Lq, Lk, masks), stream)))
         return rc;
+    uint8_t *wp = static_cast<uint8_t *>(ws.ptr);
+    a.sched = reinterpret_cast<unsigned *>(wp);
+    if ((rc = zero_sched(wp, 1, stream))) return rc;
+    wp += sched_bytes(1);
     if (masks) {
-        g.cls = static_cast<const int8_t *>(ws.ptr);
-        if ((rc = run_tile_classes(g, static_cast<int8_t *>(ws.ptr), stream))) return rc;
+        g.cls = reinterpret_cast<const int8_t *>(wp);
+        if ((rc = run_tile_classes(g, reinterpret_cast<int8_t *>(wp), stream))) return rc;
     }
     a.q = q.ptr;
     a.k = k.ptr;
@@ -711,7 +726,7 @@ size_t ring_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype, int P
     if (NC == 0 || T % NC) return 0;
     const int CL = T / NC;
     const size_t nt = (size_t)NC * ceil_div(CL, TILE);
-    size_t bytes = 0;
+    size_t bytes = sched_bytes(mode == BA_MODE_STEPWISE ? P : 1);
     if (has_masks) bytes += align256((size_t)B * nt * nt);
     const size_t tensor = (size_t)B * H * T * d;
     if (rope) bytes += 2 * align256(tensor * elem_size(dtype));
@@ -755,6 +770,10 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     const size_t need = ring_attn_fwd_workspace_size(B, H, T, d, dtype, P, partition, mode, masks, rope, out_dtype);
     if ((rc = ws.acquire(workspace, workspace_bytes, need, stream))) return rc;
     uint8_t *wp = static_cast<uint8_t *>(ws.ptr);
+    const int launches = mode == BA_MODE_STEPWISE ? P : 1;
+    unsigned *sched = reinterpret_cast<unsigned *>(wp);
+    if ((rc = zero_sched(wp, launches, stream))) return rc;
+    wp += sched_bytes(launches);
 
     AttnArgs a;
     std::memset(&a, 0, sizeof a);
@@ -811,6 +830,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     a.wait_limit_ns = kWaitLimitNs;
 
     if (mode == BA_MODE_FUSED || P == 1) {
+        a.sched = sched;
         a.out = out;
         a.out_dtype = out_dtype;
         return run_attention(a, dev, T, T, stream);
@@ -821,6 +841,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     for (int s = 0; s < P; ++s) {
         g.s_begin = s;
         g.s_end = s + 1;
+        a.sched = sched + s;
         a.acc_o = s > 0 ? acc : nullptr;
         a.acc_lse = s > 0 ? lse : nullptr;
         const bool last = s == P - 1;

@@ -1,7 +1,8 @@
 // Tensor-core attention kernel for sm_103a (bf16 Q/K/V, head dim 64 or 128).
 //
 // Persistent CTAs (one per SM) take work items = (query tile of 128 rows,
-// batch item, head).  For each item the query tile stays resident in shared
+// batch item, head), claimed one at a time from a launch-wide counter in
+// heaviest-first order (or dealt round-robin when no counter is given).  For each item the query tile stays resident in shared
 // memory while the key tiles of its walk arrive in ring order; every tile is
 // folded into a running (row max, denominator, weighted sum) that is rescaled
 // to the new maximum, never added or averaged (brunomaga "Improving numerical
@@ -22,6 +23,9 @@
 // P is double buffered so the softmax of tile j+1 overlaps the PV of tile j.
 //
 // TMEM columns: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,384+D).
+//
+// The producer passes each claimed item (index, key-tile count) to the MMA
+// thread and the softmax warps through a two-slot ring (ITEM_FULL / ITEM_EMPTY).
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // BA_ERR_TIMEOUT in the error word, drains its outstanding copies and MMAs
@@ -54,10 +58,13 @@ struct Cfg {
         B_OFULL = B_PVDONE + 2,
         B_OEMPTY,
         B_DRAIN,
-        NBAR
+        B_ITEMFULL,
+        B_ITEMEMPTY = B_ITEMFULL + 2,
+        NBAR = B_ITEMEMPTY + 2
     };
-    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort, [2..3] item tiles
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1 KB
+    // [0] tmem base, [1] abort, [2..3] item key tiles, [4..5] item index (by item parity)
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 32 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t S_COL = 0;
     static constexpr uint32_t P_COL = 256;
     static constexpr uint32_t O_COL = 384;
@@ -240,6 +247,10 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(bar(C::B_OFULL), 1);
         mbar_init(bar(C::B_OEMPTY), 128);
         mbar_init(bar(C::B_DRAIN), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_ITEMFULL + i), 1);
+            mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 4);   // MMA thread + one lane per softmax warp
+        }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -266,16 +277,28 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) {
             uint32_t fill = 0, qfills = 0, it_local = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
-                const QTile qt = work_item(g, w);
-                {
-                    // Number of key tiles of this item, for the MMA thread, counted while
-                    // the previous item still runs.  Slots alternate by item parity: slot it&1 was last read by
-                    // the MMA thread at the start of item it-2, before it committed
-                    // Q_EMPTY(it-2), which this thread waited for before loading Q(it-1).
-                    // Published by the Q_FULL arrive below.
-                    misc[2 + (it_local & 1)] = (uint32_t)kwalk_count(g, qt);
+            // Items are claimed from the launch's counter in index order (heaviest
+            // first under causal masking), so an SM takes its next item when it runs
+            // out of work; without a counter they are dealt round-robin by CTA.
+            int w = a.sched ? (int)atomicAdd(a.sched, 1u) : (int)blockIdx.x;
+            for (;; ++it_local) {
+                // Publish (item, key tiles) in slot it & 1 for the MMA thread and the
+                // softmax warps; the slot's previous item (it - 2) has been read by all.
+                const uint32_t sl = it_local & 1;
+                if (it_local >= 2 &&
+                    !mbar_wait(bar(C::B_ITEMEMPTY + sl), ((it_local >> 1) - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
                 }
+                if (w >= g.n_items) {
+                    misc[4 + sl] = 0xffffffffu;   // end of work
+                    mbar_arrive(bar(C::B_ITEMFULL + sl));
+                    break;
+                }
+                const QTile qt = work_item(g, w);
+                misc[4 + sl] = (uint32_t)w;
+                misc[2 + sl] = (uint32_t)kwalk_count(g, qt);
+                mbar_arrive(bar(C::B_ITEMFULL + sl));
                 if (it_local > 0 && !mbar_wait(bar(C::B_QEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
@@ -302,6 +325,8 @@ __global__ void __launch_bounds__(256, 1)
                                     bar(C::B_KVFULL + st));
                     ++fill;
                 }
+                if (!ok) break;
+                w = a.sched ? (int)atomicAdd(a.sched, 1u) : w + (int)gridDim.x;
             }
             if (!ok) {
                 // Let the copies already issued land before the CTA exits.
@@ -328,7 +353,15 @@ __global__ void __launch_bounds__(256, 1)
             const uint64_t qdesc0 = sdesc(sQ, 16, 1024);            // K-major, 128B swizzle
             const uint64_t kdesc0 = sdesc(sKV, 16, 1024);
             const uint64_t vdesc0 = sdesc(sKV + C::TILE_BYTES, C::BOX_BYTES, 1024);  // MN-major
-            for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
+            for (;; ++it_local) {
+                const uint32_t sl = it_local & 1;
+                if (!mbar_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t item = misc[4 + sl], n_tiles = misc[2 + sl];
+                mbar_arrive(bar(C::B_ITEMEMPTY + sl));
+                if (item == 0xffffffffu) break;
                 if (!mbar_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
@@ -340,7 +373,6 @@ __global__ void __launch_bounds__(256, 1)
                 bool o_free = it_local == 0;
                 bool first_pv = true, have_prev = false;
                 uint32_t prev_st = 0;
-                const uint32_t n_tiles = misc[2 + (it_local & 1)];
                 for (uint32_t t = 0;; ++t) {
                     const bool more = t < n_tiles;
                     uint32_t st = 0;
@@ -418,8 +450,17 @@ __global__ void __launch_bounds__(256, 1)
         const float sl2 = a.scale_log2;
         uint32_t scnt = 0, it_local = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < g.n_items && ok; w += gridDim.x, ++it_local) {
-            const QTile qt = work_item(g, w);
+        for (;; ++it_local) {
+            const uint32_t sl = it_local & 1;
+            if (!warp_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t item = misc[4 + sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
+            if (item == 0xffffffffu) break;
+            const QTile qt = work_item(g, (int)item);
             const long long qpos = qt.pos0 + row;
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;

@@ -25,6 +25,7 @@ struct AttnArgs {
     const float *acc_o;                  // nullable fp32 (B, H, rows, d) partial to merge with
     const float *acc_lse;                // nullable fp32 (B, H, rows)
     unsigned *err;                       // device error word
+    unsigned *sched;                     // nullable zeroed item counter (dynamic scheduling); null = round-robin
     unsigned long long wait_limit_ns;    // bounded-wait limit
 };
 

@@ -31,6 +31,11 @@
  *    workspace == NULL makes the library allocate it stream-ordered
  *    (cudaMallocAsync) and free it on the same stream before returning;
  *    the *_workspace_size() queries give the bytes a caller should pass.
+ *    A caller's workspace must start on a 256-byte boundary (BA_ERR_ARG
+ *    otherwise) and is used only by this call's launches on `stream`.  Its
+ *    first 256 bytes (more for many ring steps) hold the zeroed item
+ *    counters from which the attention kernel's CTAs claim work, heaviest
+ *    query tiles first, so that every SM stays busy to the end.
  *  - bf16 inputs with d in {64, 128} run on the tcgen05 tensor-core kernel
  *    (TMA-staged tiles, TMEM accumulators); fp32 inputs, and bf16 with other d
  *    in {16, 32}, run on a CUDA-core kernel that keeps fp32 arithmetic.

@@ -81,6 +81,12 @@ def test_workspace_sizes():
     # rope copies of q and k for the 64K config: 2 x 268M bf16 elements
     n = ba.ring_attn_fwd_workspace_size(1, 32, 65536, 128, __import__("torch").bfloat16, 16, "zigzag", "fused",
                                         False, True)
-    assert n == 2 * 32 * 65536 * 128 * 2
+    # plus the 256-byte block of item counters (one per launch) at the front
+    assert n == 256 + 2 * 32 * 65536 * 128 * 2
     assert ba.ring_attn_fwd_workspace_size(1, 32, 65536, 128, __import__("torch").bfloat16, 16, "zigzag",
-                                           "fused", False, False) == 0
+                                           "fused", False, False) == 256
+    # step-wise: one counter per ring step (64 steps -> 256 bytes, 65 -> 512)
+    assert ba.ring_attn_fwd_workspace_size(1, 1, 128 * 64, 64, __import__("torch").float32, 64, "contiguous",
+                                           "stepwise", False, False) == 256
+    assert ba.ring_attn_fwd_workspace_size(1, 1, 128 * 65, 64, __import__("torch").float32, 65, "contiguous",
+                                           "stepwise", False, False) == 512

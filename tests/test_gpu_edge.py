@@ -185,3 +185,25 @@ def test_bounded_wait_reports_timeout():
     out, lse = ba.ring_attn_fwd(q, q, q, P=1)
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+def test_workspace_reuse_and_alignment(mode):
+    """A caller's workspace holds the item counters the kernel claims work from:
+    they are re-zeroed by every call, so one buffer serves call after call, and a
+    workspace off a 256-byte boundary is refused before anything is launched."""
+    B, H, T, d, P = 1, 3, 1024, 128, 4
+    need = ba.ring_attn_fwd_workspace_size(B, H, T, d, torch.bfloat16, P, "zigzag", mode)
+    assert need >= 256
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+    ws.fill_(0xA5)   # counters start from garbage: the call must clear them
+    for seed in (70, 80):
+        q, k, v = (rand((B, H, T, d), torch.bfloat16, seed + i) for i in range(3))
+        out, lse = ba.ring_attn_fwd(q, k, v, P=P, partition="zigzag", mode=mode, causal=True, workspace=ws)
+        o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True)
+        compare(out, lse, o_ref, l_ref, "bf16", f"workspace reuse {mode} seed={seed}")
+    with pytest.raises(ba.BlockAttnError):
+        ba.ring_attn_fwd(q, k, v, P=P, partition="zigzag", mode=mode, causal=True, workspace=ws[16:])
+    out, lse = ba.attn_block_fwd(q, k, v, causal=True, workspace=ws, out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True)
+    compare(out, lse, o_ref, l_ref, "bf16", "block with caller workspace")

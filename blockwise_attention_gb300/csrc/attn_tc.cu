@@ -10,7 +10,8 @@
 //
 // Roles (256 threads):
 //   warp 0      TMA producer: Q tile, then K and V tiles into two stage rings
-//               (128B-swizzled boxes of 64 columns x 128 rows).
+//               (128B-swizzled boxes of 64 columns x 128 rows); K of tile j is
+//               issued before V of tile j - 1.
 //   warp 1      owns TMEM (512 columns) and issues tcgen05.mma from one thread:
 //               S = Q K^T (A, B from shared memory, fp32 accumulate in TMEM),
 //               O += P V (A = P from TMEM, B = V from shared memory).
@@ -19,10 +20,15 @@
 //               to TMEM, rescales O when the row maximum grows by more than
 //               2^8, and at the end normalises O and stores out / lse.
 //   warps 2..3  idle.
-// S is double buffered so the MMA for tile j+1 overlaps the softmax of tile j;
-// P is double buffered so the softmax of tile j+1 overlaps the PV of tile j.
+// S has three buffers and PV runs two tiles behind QK: QK(j+1) and QK(j+2)
+// are computed while the softmax works on tile j, so three tiles are in
+// flight between the tensor pipe and the softmax.  P(j) (bf16, 64 columns) is
+// written over the S buffer it was computed from; QK(j+3), the next writer of
+// that buffer, is issued after PV(j), and the tensor pipe executes in issue
+// order.  K stages are released when their QK completes, V stages when their
+// PV completes.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O [384,384+D).
+// TMEM columns: S0 [0,128) S1 [128,256) S2 [256,384) O [384,384+D).
 //
 // The producer passes each claimed item (index, key-tile count) to the MMA
 // thread and the softmax warps through a two-slot ring (ITEM_FULL / ITEM_EMPTY).
@@ -43,30 +49,38 @@ struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
     static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
-    static constexpr int NS = D == 128 ? 3 : 4;    // stages, each one K tile and one V tile
+    static constexpr int KS = D == 128 ? 3 : 5;    // K stages
+    static constexpr int VS = D == 128 ? 3 : 5;    // V stages
+    static constexpr int NSB = 3;                  // S buffers in TMEM
+    static constexpr int TIR = 8;                  // key-tile description ring (power of two)
     static constexpr int Q_OFF = 0;
-    static constexpr int KV_OFF = TILE_BYTES;      // stage i: K at KV_OFF + 2i*TILE_BYTES, V right after
-    static constexpr int BAR_OFF = KV_OFF + NS * 2 * TILE_BYTES;
+    static constexpr int K_OFF = TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
+    static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
     enum {
         B_QFULL = 0,
         B_QEMPTY,
-        B_KVFULL,
-        B_KVEMPTY = B_KVFULL + NS,
-        B_SFULL = B_KVEMPTY + NS,
-        B_PFULL = B_SFULL + 2,
-        B_PVDONE = B_PFULL + 2,
-        B_OFULL = B_PVDONE + 2,
+        B_KFULL,
+        B_KEMPTY = B_KFULL + KS,
+        B_VFULL = B_KEMPTY + KS,
+        B_VEMPTY = B_VFULL + VS,
+        B_SFULL = B_VEMPTY + VS,
+        B_PFULL = B_SFULL + NSB,
+        B_PVDONE = B_PFULL + NSB,
+        B_OFULL = B_PVDONE + NSB,
         B_OEMPTY,
         B_DRAIN,
         B_ITEMFULL,
         B_ITEMEMPTY = B_ITEMFULL + 2,
-        NBAR = B_ITEMEMPTY + 2
+        B_TIFULL = B_ITEMEMPTY + 2,   // key-tile descriptions for the softmax warps
+        B_TIEMPTY = B_TIFULL + TIR,
+        NBAR = B_TIEMPTY + TIR
     };
     // [0] tmem base, [1] abort, [2..3] item key tiles, [4..5] item index (by item parity)
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int SMEM_BYTES = MISC_OFF + 32 + 1024;  // + slack to align the base to 1 KB
-    static constexpr uint32_t S_COL = 0;
-    static constexpr uint32_t P_COL = 256;
+    static constexpr int TI_OFF = MISC_OFF + 32;            // TIR x uint2 {global position, len | class << 16}
+    static constexpr int SMEM_BYTES = TI_OFF + TIR * 8 + 1024;  // + slack to align the base to 1 KB
+    static constexpr uint32_t S_COL = 0;     // S buffer b at S_COL + 128 b; P over its first 64 columns
     static constexpr uint32_t O_COL = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     // Instruction descriptors (kind::f16): D fp32 (bits 4-5 = 1), A and B
@@ -112,6 +126,33 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The MMA warp runs converged; these issue from one elected lane, so that
+// descriptors and addresses stay warp-uniform values.
+__device__ __forceinline__ void mma_ss_one(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_one(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_one(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
 
@@ -186,7 +227,9 @@ __device__ __forceinline__ void mask_bytes(const uint8_t *p, int n, float *s) {
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = 0;
-        for (int i = 0; i < n && i < 32; ++i) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < n) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -222,10 +265,11 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw_base);
-    const uint32_t sQ = base + C::Q_OFF, sKV = base + C::KV_OFF;
+    const uint32_t sQ = base + C::Q_OFF, sK = base + C::K_OFF, sV = base + C::V_OFF;
     const uint32_t bars = base + C::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
+    volatile uint2 *tinfo = reinterpret_cast<volatile uint2 *>(gbase + C::TI_OFF);
     volatile int *abort = reinterpret_cast<volatile int *>(gbase + C::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,11 +279,15 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QEMPTY), 1);
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(bar(C::B_KVFULL + i), 1);
-            mbar_init(bar(C::B_KVEMPTY + i), 1);
+        for (int i = 0; i < C::KS; ++i) {
+            mbar_init(bar(C::B_KFULL + i), 1);
+            mbar_init(bar(C::B_KEMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::VS; ++i) {
+            mbar_init(bar(C::B_VFULL + i), 1);
+            mbar_init(bar(C::B_VEMPTY + i), 1);
+        }
+        for (int i = 0; i < C::NSB; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
             mbar_init(bar(C::B_PFULL + i), 128);
             mbar_init(bar(C::B_PVDONE + i), 1);
@@ -249,7 +297,11 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(bar(C::B_DRAIN), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::B_ITEMFULL + i), 1);
-            mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 4);   // MMA thread + one lane per softmax warp
+            mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 4);   // MMA warp + one lane per softmax warp
+        }
+        for (int i = 0; i < C::TIR; ++i) {
+            mbar_init(bar(C::B_TIFULL + i), 1);
+            mbar_init(bar(C::B_TIEMPTY + i), 4);          // one lane per softmax warp
         }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -275,7 +327,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t fill = 0, qfills = 0, it_local = 0;
+            uint32_t kfill = 0, vfill = 0, qfills = 0, it_local = 0;
             bool ok = true;
             // Items are claimed from the launch's counter in index order (heaviest
             // first under causal masking), so an SM takes its next item when it runs
@@ -310,20 +362,45 @@ __global__ void __launch_bounds__(256, 1)
                 KWalk wk;
                 kwalk_begin(g, qt, wk);
                 KTile kt;
-                while (kwalk_next(g, qt, wk, kt)) {
-                    const uint32_t st = fill % C::NS, use = fill / C::NS;
-                    if (use > 0 && !mbar_wait(bar(C::B_KVEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
+                int prev_row = -1;   // k/v row of the tile whose V is still to be loaded
+                for (;;) {
+                    const bool more = kwalk_next(g, qt, wk, kt);
+                    if (more) {
+                        // Describe the tile for the softmax warps (slot kfill % TIR, free
+                        // once they have read the tile TIR places earlier).
+                        const uint32_t ts = kfill % C::TIR, tuse = kfill / C::TIR;
+                        if (tuse > 0 && !mbar_wait(bar(C::B_TIEMPTY + ts), (tuse - 1) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        tinfo[ts].x = (uint32_t)kt.pos0;
+                        tinfo[ts].y = (uint32_t)kt.len | ((uint32_t)kt.cls << 16);
+                        mbar_arrive(bar(C::B_TIFULL + ts));
+                        const uint32_t st = kfill % C::KS, use = kfill / C::KS;
+                        if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
+                        for (int bx = 0; bx < C::NBOX; ++bx)
+                            tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h,
+                                        qt.b, bar(C::B_KFULL + st));
+                        ++kfill;
                     }
-                    const uint32_t dst = sKV + st * 2 * C::TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::TILE_BYTES);
-                    for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_4d(dst + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h, qt.b, bar(C::B_KVFULL + st));
-                    for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_4d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, kt.row0, qt.h, qt.b,
-                                    bar(C::B_KVFULL + st));
-                    ++fill;
+                    if (prev_row >= 0) {
+                        const uint32_t st = vfill % C::VS, use = vfill / C::VS;
+                        if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
+                        for (int bx = 0; bx < C::NBOX; ++bx)
+                            tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, prev_row, qt.h,
+                                        qt.b, bar(C::B_VFULL + st));
+                        ++vfill;
+                    }
+                    if (!more) break;
+                    prev_row = kt.row0;
                 }
                 if (!ok) break;
                 w = a.sched ? (int)atomicAdd(a.sched, 1u) : w + (int)gridDim.x;
@@ -333,36 +410,45 @@ __global__ void __launch_bounds__(256, 1)
                 volatile int never = 0;
                 const uint64_t lim2 = 200000000ull;
                 if (qfills > 0) mbar_wait(bar(C::B_QFULL), (qfills - 1) & 1, &never, nullptr, lim2);
-                for (uint32_t i = 0; i < (uint32_t)C::NS && i < fill; ++i) {
-                    const uint32_t last = fill - 1 - i;
-                    mbar_wait(bar(C::B_KVFULL + last % C::NS), (last / C::NS) & 1, &never, nullptr, lim2);
+                for (uint32_t i = 0; i < (uint32_t)C::KS && i < kfill; ++i) {
+                    const uint32_t last = kfill - 1 - i;
+                    mbar_wait(bar(C::B_KFULL + last % C::KS), (last / C::KS) & 1, &never, nullptr, lim2);
+                }
+                for (uint32_t i = 0; i < (uint32_t)C::VS && i < vfill; ++i) {
+                    const uint32_t last = vfill - 1 - i;
+                    mbar_wait(bar(C::B_VFULL + last % C::VS), (last / C::VS) & 1, &never, nullptr, lim2);
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Per key tile j: wait K/V of j, QK(j) -> S[j % 2], then PV(j - 1) once the
-        // softmax has written P(j - 1).  QK(j + 1) is therefore issued only after
-        // P(j - 1) exists, which implies S(j - 1) was read: no separate "S free"
-        // barrier is needed.  The S_FULL(j) commit covers every earlier MMA, so the
-        // softmax may overwrite P(j % 2) (last read by PV(j - 2)) once S(j) is full.
-        if (lane == 0) {
-            uint32_t cons = 0, scnt = 0, pcnt = 0, it_local = 0;
+        // Per key tile j: wait K of j, QK(j) -> S[j % 3], then PV(j - 2) once the
+        // softmax has written P(j - 2) and V(j - 2) has landed.  QK(j) overwrites
+        // the buffer that held P(j - 3), which PV(j - 3), issued one step
+        // earlier, has read: the tensor pipe executes in issue order, so no
+        // separate "S free" barrier is needed.
+        // The whole warp runs this loop converged (waits, counters, descriptors);
+        // each MMA and commit is issued by one elected lane.
+        {
+            uint32_t kcons = 0, vcons = 0, it_local = 0;
+            uint32_t qb = 0, qph = 0;   // S buffer and phase of the next QK
+            uint32_t pb = 0, pph = 0;   // S buffer and phase of the next PV
             bool ok = true;
             const uint64_t qdesc0 = sdesc(sQ, 16, 1024);            // K-major, 128B swizzle
-            const uint64_t kdesc0 = sdesc(sKV, 16, 1024);
-            const uint64_t vdesc0 = sdesc(sKV + C::TILE_BYTES, C::BOX_BYTES, 1024);  // MN-major
+            const uint64_t kdesc0 = sdesc(sK, 16, 1024);
+            const uint64_t vdesc0 = sdesc(sV, C::BOX_BYTES, 1024);   // MN-major
             for (;; ++it_local) {
                 const uint32_t sl = it_local & 1;
-                if (!mbar_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
+                if (!warp_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
                 const uint32_t item = misc[4 + sl], n_tiles = misc[2 + sl];
-                mbar_arrive(bar(C::B_ITEMEMPTY + sl));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
                 if (item == 0xffffffffu) break;
-                if (!mbar_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
+                if (!warp_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
@@ -371,41 +457,43 @@ __global__ void __launch_bounds__(256, 1)
                 // writes O or signals O_FULL: waited exactly once per item, so the
                 // O_FULL / O_EMPTY phases never run two ahead of their waiters.
                 bool o_free = it_local == 0;
-                bool first_pv = true, have_prev = false;
-                uint32_t prev_st = 0;
-                for (uint32_t t = 0;; ++t) {
-                    const bool more = t < n_tiles;
-                    uint32_t st = 0;
-                    if (more) {
-                        st = cons % C::NS;
-                        // TMA data is ordered by the barrier itself; S[scnt & 1] was last
-                        // read by the softmax of tile j - 2, ordered by P_FULL(j - 2) below.
-                        if (!mbar_wait(bar(C::B_KVFULL + st), (cons / C::NS) & 1, abort, a.err, lim)) {
+                bool first_pv = true;
+                if (n_tiles == 0) mma_commit_one(bar(C::B_QEMPTY));
+                for (uint32_t t = 0; t < n_tiles + 2; ++t) {
+                    if (t < n_tiles) {
+                        const uint32_t st = kcons % C::KS;
+                        if (!warp_wait(bar(C::B_KFULL + st), (kcons / C::KS) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
-                        const uint64_t kd = kdesc0 + (uint64_t)((st * 2 * C::TILE_BYTES) >> 4);
-                        const uint32_t sd = tmem + C::S_COL + (scnt & 1) * 128;
+                        tc_fence_after();
+                        const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
+                        const uint32_t sd = tmem + C::S_COL + qb * 128;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                            mma_ss(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                            mma_ss_one(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(C::B_SFULL + (scnt & 1)));
-                        ++cons;
-                        ++scnt;
-                    } else {
-                        mma_commit(bar(C::B_QEMPTY));   // every QK of the item is issued
+                        mma_commit_one(bar(C::B_SFULL + qb));
+                        mma_commit_one(bar(C::B_KEMPTY + st));
+                        if (t + 1 == n_tiles) mma_commit_one(bar(C::B_QEMPTY));   // every QK of the item is issued
+                        ++kcons;
+                        qb = qb == C::NSB - 1 ? 0 : qb + 1;
+                        qph ^= qb == 0;
                     }
-                    if (have_prev) {
-                        // PV of the previous tile
-                        const uint32_t pb = pcnt & 1;
-                        if (!mbar_wait(bar(C::B_PFULL + pb), (pcnt >> 1) & 1, abort, a.err, lim)) {
+                    if (t >= 2) {
+                        // PV of tile t - 2
+                        if (!warp_wait(bar(C::B_PFULL + pb), pph, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t st = vcons % C::VS;
+                        if (!warp_wait(bar(C::B_VFULL + st), (vcons / C::VS) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
                         if (!o_free) {
-                            if (!mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
+                            if (!warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                                 ok = false;
                                 break;
                             }
@@ -413,33 +501,32 @@ __global__ void __launch_bounds__(256, 1)
                         }
                         tc_fence_after();
                         // descriptor start-address field advances by bytes / 16
-                        const uint64_t vd = vdesc0 + (uint64_t)((prev_st * 2 * C::TILE_BYTES) >> 4);
-                        const uint32_t pa = tmem + C::P_COL + pb * 64;
+                        const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
+                        const uint32_t pa = tmem + C::S_COL + pb * 128;
 #pragma unroll
                         for (int kk = 0; kk < TILE / 16; ++kk)
-                            mma_ts(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
+                            mma_ts_one(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
                                    (first_pv && kk == 0) ? 0u : 1u);
-                        mma_commit(bar(C::B_KVEMPTY + prev_st));
-                        mma_commit(bar(C::B_PVDONE + pb));
-                        ++pcnt;
+                        mma_commit_one(bar(C::B_VEMPTY + st));
+                        mma_commit_one(bar(C::B_PVDONE + pb));
+                        ++vcons;
+                        pb = pb == C::NSB - 1 ? 0 : pb + 1;
+                        pph ^= pb == 0;
                         first_pv = false;
                     }
-                    have_prev = more;
-                    prev_st = st;
-                    if (!more) break;
                 }
                 if (!ok) break;
-                if (!o_free && !mbar_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
+                if (!o_free && !warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
-                mma_commit(bar(C::B_OFULL));
+                mma_commit_one(bar(C::B_OFULL));
             }
             if (!ok) {
                 // Wait for the MMAs already issued before TMEM is released.
                 volatile int never = 0;
-                mma_commit(bar(C::B_DRAIN));
-                mbar_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
+                mma_commit_one(bar(C::B_DRAIN));
+                warp_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
             }
         }
         __syncwarp();
@@ -448,7 +535,10 @@ __global__ void __launch_bounds__(256, 1)
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_addr = ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = a.scale_log2;
-        uint32_t scnt = 0, it_local = 0;
+        uint32_t it_local = 0;
+        uint32_t sb = 0, sph = 0;   // S buffer and phase of the next tile
+        uint32_t pvb = 0, pvph = 0; // S buffer and phase of the previous tile (valid once n > 0)
+        uint32_t tcnt = 0;          // key tiles described so far (ring position)
         bool ok = true;
         for (;; ++it_local) {
             const uint32_t sl = it_local & 1;
@@ -456,7 +546,7 @@ __global__ void __launch_bounds__(256, 1)
                 ok = false;
                 break;
             }
-            const uint32_t item = misc[4 + sl];
+            const uint32_t item = misc[4 + sl], n_tiles = misc[2 + sl];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
             if (item == 0xffffffffu) break;
@@ -464,12 +554,24 @@ __global__ void __launch_bounds__(256, 1)
             const long long qpos = qt.pos0 + row;
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;
-            KWalk wk;
-            kwalk_begin(g, qt, wk);
-            KTile kt;
-            while (kwalk_next(g, qt, wk, kt)) {
-                const uint32_t sb = scnt & 1;
-                if (!warp_wait(bar(C::B_SFULL + sb), (scnt >> 1) & 1, abort, a.err, lim)) {
+            for (uint32_t j = 0; j < n_tiles; ++j) {
+                // The producer walked the tiles; take this one's position, length and class.
+                KTile kt;
+                {
+                    const uint32_t ts = tcnt % C::TIR;
+                    if (!warp_wait(bar(C::B_TIFULL + ts), (tcnt / C::TIR) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dx = tinfo[ts].x, dy = tinfo[ts].y;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_TIEMPTY + ts));
+                    ++tcnt;
+                    kt.pos0 = (long long)dx;
+                    kt.len = (int)(dy & 0xffffu);
+                    kt.cls = (int)(dy >> 16);
+                }
+                if (!warp_wait(bar(C::B_SFULL + sb), sph, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
@@ -521,14 +623,14 @@ __global__ void __launch_bounds__(256, 1)
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;
 
-                const uint32_t pb = scnt & 1;   // last read by PV(j - 2), complete once S(j) is full
+                // P over the first 64 columns of the S buffer just read
 #pragma unroll
                 for (int c = 0; c < TILE / 64; ++c)
-                    tmem_st32(tmem + lane_addr + C::P_COL + pb * 64 + c * 32,
+                    tmem_st32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32,
                               *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
-                    const uint32_t prev = scnt - 1;
-                    if (!warp_wait(bar(C::B_PVDONE + (prev & 1)), (prev >> 1) & 1, abort, a.err, lim)) {
+                    // O may be rescaled once PV of the previous tile has completed
+                    if (!warp_wait(bar(C::B_PVDONE + pvb), pvph, abort, a.err, lim)) {
                         ok = false;
                         break;
                     }
@@ -545,8 +647,11 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL + pb));
-                ++scnt;
+                mbar_arrive(bar(C::B_PFULL + sb));
+                pvb = sb;
+                pvph = sph;
+                sb = sb == C::NSB - 1 ? 0 : sb + 1;
+                sph ^= sb == 0;
                 ++n;
             }
             if (!ok) break;

@@ -49,9 +49,12 @@ struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
     static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
-    static constexpr int KS = D == 128 ? 3 : 5;    // K stages
-    static constexpr int VS = D == 128 ? 3 : 5;    // V stages
+    // One K stage and one V stage per S buffer: tile j uses K stage, V stage
+    // and S buffer j % 3, so the S_FULL commit of QK(j) also frees K stage
+    // j % 3 and the PV_DONE commit of PV(j) frees V stage j % 3.
     static constexpr int NSB = 3;                  // S buffers in TMEM
+    static constexpr int KS = NSB;                 // K stages
+    static constexpr int VS = NSB;                 // V stages
     static constexpr int TIR = 8;                  // key-tile description ring (power of two)
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = TILE_BYTES;
@@ -61,12 +64,10 @@ struct Cfg {
         B_QFULL = 0,
         B_QEMPTY,
         B_KFULL,
-        B_KEMPTY = B_KFULL + KS,
-        B_VFULL = B_KEMPTY + KS,
-        B_VEMPTY = B_VFULL + VS,
-        B_SFULL = B_VEMPTY + VS,
+        B_VFULL = B_KFULL + KS,
+        B_SFULL = B_VFULL + VS,     // QK(j) complete: S ready, K stage j % 3 free
         B_PFULL = B_SFULL + NSB,
-        B_PVDONE = B_PFULL + NSB,
+        B_PVDONE = B_PFULL + NSB,   // PV(j) complete: V stage j % 3 free, O may be rescaled
         B_OFULL = B_PVDONE + NSB,
         B_OEMPTY,
         B_DRAIN,
@@ -279,14 +280,8 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QEMPTY), 1);
-        for (int i = 0; i < C::KS; ++i) {
-            mbar_init(bar(C::B_KFULL + i), 1);
-            mbar_init(bar(C::B_KEMPTY + i), 1);
-        }
-        for (int i = 0; i < C::VS; ++i) {
-            mbar_init(bar(C::B_VFULL + i), 1);
-            mbar_init(bar(C::B_VEMPTY + i), 1);
-        }
+        for (int i = 0; i < C::KS; ++i) mbar_init(bar(C::B_KFULL + i), 1);
+        for (int i = 0; i < C::VS; ++i) mbar_init(bar(C::B_VFULL + i), 1);
         for (int i = 0; i < C::NSB; ++i) {
             mbar_init(bar(C::B_SFULL + i), 1);
             mbar_init(bar(C::B_PFULL + i), 128);
@@ -377,7 +372,7 @@ __global__ void __launch_bounds__(256, 1)
                         tinfo[ts].y = (uint32_t)kt.len | ((uint32_t)kt.cls << 16);
                         mbar_arrive(bar(C::B_TIFULL + ts));
                         const uint32_t st = kfill % C::KS, use = kfill / C::KS;
-                        if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                        if (use > 0 && !mbar_wait(bar(C::B_SFULL + st), (use - 1) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
@@ -389,7 +384,7 @@ __global__ void __launch_bounds__(256, 1)
                     }
                     if (prev_row >= 0) {
                         const uint32_t st = vfill % C::VS, use = vfill / C::VS;
-                        if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                        if (use > 0 && !mbar_wait(bar(C::B_PVDONE + st), (use - 1) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
@@ -423,28 +418,59 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Per key tile j: wait K of j, QK(j) -> S[j % 3], then PV(j - 2) once the
-        // softmax has written P(j - 2) and V(j - 2) has landed.  QK(j) overwrites
-        // the buffer that held P(j - 3), which PV(j - 3), issued one step
-        // earlier, has read: the tensor pipe executes in issue order, so no
+        // Per key tile j: QK(j) -> S[j % 3] once K(j) has landed, and PV(j - 2)
+        // once the softmax has written P(j - 2) and V(j - 2) has landed.  QK(j)
+        // overwrites the buffer that held P(j - 3), which PV(j - 3), issued just
+        // before, has read: the tensor pipe executes in issue order, so no
         // separate "S free" barrier is needed.
         // The whole warp runs this loop converged (waits, counters, descriptors);
         // each MMA and commit is issued by one elected lane.
         {
-            uint32_t kcons = 0, vcons = 0, it_local = 0;
-            uint32_t qb = 0, qph = 0;   // S buffer and phase of the next QK
-            uint32_t pb = 0, pph = 0;   // S buffer and phase of the next PV
+            uint32_t it_local = 0;
+            uint32_t qb = 0, qph = 0;   // buffer / stage index and phase of the next QK
+            uint32_t pb = 0, pph = 0;   // buffer / stage index and phase of the next PV
             bool ok = true;
             const uint64_t qdesc0 = sdesc(sQ, 16, 1024);            // K-major, 128B swizzle
             const uint64_t kdesc0 = sdesc(sK, 16, 1024);
             const uint64_t vdesc0 = sdesc(sV, C::BOX_BYTES, 1024);   // MN-major
+            // descriptor start-address fields advance by bytes / 16
+            constexpr uint32_t STAGE16 = C::TILE_BYTES >> 4;
+            auto qk = [&]() -> bool {
+                if (!warp_wait(bar(C::B_KFULL + qb), qph, abort, a.err, lim)) return false;
+                const uint64_t kd = kdesc0 + (uint64_t)(qb * STAGE16);
+                const uint32_t sd = tmem + C::S_COL + qb * 128;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                    mma_ss_one(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_one(bar(C::B_SFULL + qb));
+                qb = qb == C::NSB - 1 ? 0 : qb + 1;
+                qph ^= qb == 0;
+                return true;
+            };
+            auto pv = [&](bool first) -> bool {
+                if (!warp_wait(bar(C::B_PFULL + pb), pph, abort, a.err, lim)) return false;
+                if (!warp_wait(bar(C::B_VFULL + pb), pph, abort, a.err, lim)) return false;
+                tc_fence_after();   // P was written by the softmax warps' tcgen05.st
+                const uint64_t vd = vdesc0 + (uint64_t)(pb * STAGE16);
+                const uint32_t pa = tmem + C::S_COL + pb * 128;
+#pragma unroll
+                for (int kk = 0; kk < TILE / 16; ++kk)
+                    mma_ts_one(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
+                               (first && kk == 0) ? 0u : 1u);
+                mma_commit_one(bar(C::B_PVDONE + pb));
+                pb = pb == C::NSB - 1 ? 0 : pb + 1;
+                pph ^= pb == 0;
+                return true;
+            };
             for (;; ++it_local) {
                 const uint32_t sl = it_local & 1;
                 if (!warp_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
-                const uint32_t item = misc[4 + sl], n_tiles = misc[2 + sl];
+                const uint32_t item = misc[4 + sl], n = misc[2 + sl];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
                 if (item == 0xffffffffu) break;
@@ -452,74 +478,25 @@ __global__ void __launch_bounds__(256, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                // O of the previous item must have been read out before this item
-                // writes O or signals O_FULL: waited exactly once per item, so the
-                // O_FULL / O_EMPTY phases never run two ahead of their waiters.
-                bool o_free = it_local == 0;
-                bool first_pv = true;
-                if (n_tiles == 0) mma_commit_one(bar(C::B_QEMPTY));
-                for (uint32_t t = 0; t < n_tiles + 2; ++t) {
-                    if (t < n_tiles) {
-                        const uint32_t st = kcons % C::KS;
-                        if (!warp_wait(bar(C::B_KFULL + st), (kcons / C::KS) & 1, abort, a.err, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
-                        const uint32_t sd = tmem + C::S_COL + qb * 128;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                            mma_ss_one(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit_one(bar(C::B_SFULL + qb));
-                        mma_commit_one(bar(C::B_KEMPTY + st));
-                        if (t + 1 == n_tiles) mma_commit_one(bar(C::B_QEMPTY));   // every QK of the item is issued
-                        ++kcons;
-                        qb = qb == C::NSB - 1 ? 0 : qb + 1;
-                        qph ^= qb == 0;
-                    }
-                    if (t >= 2) {
-                        // PV of tile t - 2
-                        if (!warp_wait(bar(C::B_PFULL + pb), pph, abort, a.err, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t st = vcons % C::VS;
-                        if (!warp_wait(bar(C::B_VFULL + st), (vcons / C::VS) & 1, abort, a.err, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        if (!o_free) {
-                            if (!warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
-                                ok = false;
-                                break;
-                            }
-                            o_free = true;
-                        }
-                        tc_fence_after();
-                        // descriptor start-address field advances by bytes / 16
-                        const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
-                        const uint32_t pa = tmem + C::S_COL + pb * 128;
-#pragma unroll
-                        for (int kk = 0; kk < TILE / 16; ++kk)
-                            mma_ts_one(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
-                                   (first_pv && kk == 0) ? 0u : 1u);
-                        mma_commit_one(bar(C::B_VEMPTY + st));
-                        mma_commit_one(bar(C::B_PVDONE + pb));
-                        ++vcons;
-                        pb = pb == C::NSB - 1 ? 0 : pb + 1;
-                        pph ^= pb == 0;
-                        first_pv = false;
-                    }
+                // QK(0), QK(1); Q_EMPTY is committed right after the item's last QK.
+                if (n == 0) mma_commit_one(bar(C::B_QEMPTY));
+                if (n >= 1 && !(ok = qk())) break;
+                if (n == 1) mma_commit_one(bar(C::B_QEMPTY));
+                if (n >= 2 && !(ok = qk())) break;
+                if (n == 2) mma_commit_one(bar(C::B_QEMPTY));
+                // O of the previous item must have been read out before this item's
+                // first PV writes O (and before O_FULL): waited once per item, so
+                // the O_FULL / O_EMPTY phases never run two ahead of their waiters.
+                if (it_local > 0 && !(ok = warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)))
+                    break;
+                for (uint32_t t = 2; t < n; ++t) {
+                    if (!(ok = qk())) break;
+                    if (t + 1 == n) mma_commit_one(bar(C::B_QEMPTY));
+                    if (!(ok = pv(t == 2))) break;
                 }
                 if (!ok) break;
-                if (!o_free && !warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
-                    ok = false;
-                    break;
-                }
+                if (n >= 2 && !(ok = pv(n == 2))) break;
+                if (n >= 1 && !(ok = pv(n == 1))) break;
                 mma_commit_one(bar(C::B_OFULL));
             }
             if (!ok) {

@@ -55,7 +55,7 @@ struct Cfg {
     static constexpr int NSB = 3;                  // S buffers in TMEM
     static constexpr int KS = NSB;                 // K stages
     static constexpr int VS = NSB;                 // V stages
-    static constexpr int TIR = 8;                  // key-tile description ring (power of two)
+    static constexpr int TIR = 16;                 // key-tile description ring (power of two)
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
@@ -73,14 +73,13 @@ struct Cfg {
         B_DRAIN,
         B_ITEMFULL,
         B_ITEMEMPTY = B_ITEMFULL + 2,
-        B_TIFULL = B_ITEMEMPTY + 2,   // key-tile descriptions for the softmax warps
-        B_TIEMPTY = B_TIFULL + TIR,
-        NBAR = B_TIEMPTY + TIR
+        NBAR = B_ITEMEMPTY + 2
     };
     // [0] tmem base, [1] abort, [2..3] item key tiles, [4..5] item index (by item parity)
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int TI_OFF = MISC_OFF + 32;            // TIR x uint2 {global position, len | class << 16}
-    static constexpr int SMEM_BYTES = TI_OFF + TIR * 8 + 1024;  // + slack to align the base to 1 KB
+    // TIR x {global position, len | class << 16, tile sequence number + 1, unused}
+    static constexpr int TI_OFF = MISC_OFF + 32;
+    static constexpr int SMEM_BYTES = TI_OFF + TIR * 16 + 1024;  // + slack to align the base to 1 KB
     static constexpr uint32_t S_COL = 0;     // S buffer b at S_COL + 128 b; P over its first 64 columns
     static constexpr uint32_t O_COL = 384;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -203,12 +202,69 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait (every lane of a warp) until the shared word at addr equals
+// want; the acquire load orders the reads that follow.  Warp-uniform verdict.
+__device__ __forceinline__ bool warp_wait_seq(uint32_t addr, uint32_t want, volatile int *abort, unsigned *err,
+                                              uint64_t lim) {
+    bool ok = ld_acquire_shared(addr) == want;
+    if (!__all_sync(0xffffffffu, ok)) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t n = 1;; ++n) {
+            ok = ld_acquire_shared(addr) == want;
+            if (__all_sync(0xffffffffu, ok)) break;
+            if ((n & 63) == 0) {
+                bool stop = *abort != 0;
+                if (!stop && global_timer_ns() - t0 > lim) {
+                    *abort = 1;
+                    if (err) atomicOr(err, ERR_TIMEOUT_BIT);
+                    stop = true;
+                }
+                if (__any_sync(0xffffffffu, stop)) return false;
+            }
+        }
+    }
+    return true;
+}
+
 // Bounded wait by every lane of a warp, with a warp-uniform verdict so that
 // the warp reaches the following .sync.aligned TMEM instructions converged.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort, unsigned *err,
                                           uint64_t lim) {
     const bool ok = mbar_wait(bar, parity, abort, err, lim);
     return __all_sync(0xffffffffu, ok);
+}
+
+// max(a, b, c) in one instruction (sm_100 three-input form).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two lanes of fp32 per instruction: (d0, d1) = (a0 * b + c, a1 * b + c), each an
+// IEEE fma rounded to nearest, and (s0, s1) += (x0, x1).
+__device__ __forceinline__ void ffma2_bc(float a0, float a1, float b, float c, float &d0, float &d1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+__device__ __forceinline__ void fadd2_acc(float &s0, float &s1, float x0, float x1) {
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(s0), "+f"(s1) : "f"(x0), "f"(x1));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -270,7 +326,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t bars = base + C::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
-    volatile uint2 *tinfo = reinterpret_cast<volatile uint2 *>(gbase + C::TI_OFF);
+    volatile uint32_t *tinfo = reinterpret_cast<volatile uint32_t *>(gbase + C::TI_OFF);
+    const uint32_t sTI = base + C::TI_OFF;
     volatile int *abort = reinterpret_cast<volatile int *>(gbase + C::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -294,10 +351,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(bar(C::B_ITEMFULL + i), 1);
             mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 4);   // MMA warp + one lane per softmax warp
         }
-        for (int i = 0; i < C::TIR; ++i) {
-            mbar_init(bar(C::B_TIFULL + i), 1);
-            mbar_init(bar(C::B_TIEMPTY + i), 4);          // one lane per softmax warp
-        }
+        for (int i = 0; i < C::TIR; ++i) tinfo[4 * i + 2] = 0xffffffffu;   // no tile yet
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -361,20 +415,20 @@ __global__ void __launch_bounds__(256, 1)
                 for (;;) {
                     const bool more = kwalk_next(g, qt, wk, kt);
                     if (more) {
-                        // Describe the tile for the softmax warps (slot kfill % TIR, free
-                        // once they have read the tile TIR places earlier).
-                        const uint32_t ts = kfill % C::TIR, tuse = kfill / C::TIR;
-                        if (tuse > 0 && !mbar_wait(bar(C::B_TIEMPTY + ts), (tuse - 1) & 1, abort, a.err, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        tinfo[ts].x = (uint32_t)kt.pos0;
-                        tinfo[ts].y = (uint32_t)kt.len | ((uint32_t)kt.cls << 16);
-                        mbar_arrive(bar(C::B_TIFULL + ts));
                         const uint32_t st = kfill % C::KS, use = kfill / C::KS;
                         if (use > 0 && !mbar_wait(bar(C::B_SFULL + st), (use - 1) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
+                        }
+                        // Describe tile kfill for the softmax warps in slot kfill % TIR.  QK of
+                        // tile kfill - 3 has completed (the wait above), so the softmax has
+                        // finished tile kfill - 6 (QK(j) is issued after PV(j - 3)) and has
+                        // read every description older than that, including this slot's last.
+                        {
+                            const uint32_t e = (kfill % C::TIR) * 4;
+                            tinfo[e] = (uint32_t)kt.pos0;
+                            tinfo[e + 1] = (uint32_t)kt.len | ((uint32_t)kt.cls << 16);
+                            st_release_shared(sTI + e * 4 + 8, kfill + 1);
                         }
                         mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
@@ -532,25 +586,24 @@ __global__ void __launch_bounds__(256, 1)
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;
             for (uint32_t j = 0; j < n_tiles; ++j) {
-                // The producer walked the tiles; take this one's position, length and class.
+                if (!warp_wait(bar(C::B_SFULL + sb), sph, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                // The producer walked the tiles; take this one's position, length and
+                // class (written before K of the tile was loaded, so normally present).
                 KTile kt;
                 {
-                    const uint32_t ts = tcnt % C::TIR;
-                    if (!warp_wait(bar(C::B_TIFULL + ts), (tcnt / C::TIR) & 1, abort, a.err, lim)) {
+                    const uint32_t e = (tcnt % C::TIR) * 4;
+                    if (!warp_wait_seq(sTI + e * 4 + 8, tcnt + 1, abort, a.err, lim)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dx = tinfo[ts].x, dy = tinfo[ts].y;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_TIEMPTY + ts));
+                    const uint32_t dx = tinfo[e], dy = tinfo[e + 1];
                     ++tcnt;
                     kt.pos0 = (long long)dx;
                     kt.len = (int)(dy & 0xffffu);
                     kt.cls = (int)(dy >> 16);
-                }
-                if (!warp_wait(bar(C::B_SFULL + sb), sph, abort, a.err, lim)) {
-                    ok = false;
-                    break;
                 }
                 tc_fence_after();
                 float s[TILE];
@@ -570,14 +623,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int c = 0; c < TILE / 32; ++c) mask_chunk(g, qt.b, qpos, row_valid, kt, c * 32, &s[c * 32]);
                 }
-                // row maximum: 8 independent chains, then a tree
+                // row maximum: 8 independent chains of three-input maxima, then a tree
                 float mc[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mc[k] = s[k];
+                for (int k = 0; k < 8; ++k) mc[k] = fmaxf(s[k], s[8 + k]);
 #pragma unroll
-                for (int j = 8; j < TILE; ++j) mc[j & 7] = fmaxf(mc[j & 7], s[j]);
-                const float mx = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
-                                       fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+                for (int j = 16; j < TILE; j += 16) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], s[j + k], s[j + 8 + k]);
+                }
+                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), fmax3(fmax3(mc[3], mc[4], mc[5]), mc[6], mc[7]));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool resc = m_new > m_ref + 8.0f;   // true when m_ref = -inf and m_new finite
                 float alpha = 1.f;
@@ -586,15 +641,19 @@ __global__ void __launch_bounds__(256, 1)
                     m_ref = m_new;
                 }
                 const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                // p = 2^(s * scale * log2(e) - m): arguments two lanes at a time, the
+                // running sums in four two-lane accumulators
                 float sc[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) sc[k] = 0.f;
                 uint32_t pk[TILE / 2];
 #pragma unroll
                 for (int j = 0; j < TILE / 2; ++j) {
-                    const float p0 = fast_exp2(fmaf(s[2 * j], sl2, -m_use));
-                    const float p1 = fast_exp2(fmaf(s[2 * j + 1], sl2, -m_use));
-                    sc[j & 7] += p0 + p1;
+                    float x0, x1;
+                    ffma2_bc(s[2 * j], s[2 * j + 1], sl2, -m_use, x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    fadd2_acc(sc[2 * (j & 3)], sc[2 * (j & 3) + 1], p0, p1);
                     pk[j] = pack_bf16(p0, p1);
                 }
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));

@@ -623,6 +623,28 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int c = 0; c < TILE / 32; ++c) mask_chunk(g, qt.b, qpos, row_valid, kt, c * 32, &s[c * 32]);
                 }
+                // p = 2^(s * scale * log2(e) - m) with m the running reference maximum,
+                // computed before this tile's maximum is known: the lazy rule keeps m
+                // unless the tile's maximum exceeds it by more than 2^8, so the tile
+                // maximum (ALU pipe) and the exponentials (MUFU / FMA pipes) run side by
+                // side, and only a row whose maximum did move redoes its exponentials.
+                // Arguments two lanes at a time, sums in four two-lane accumulators.
+                float sc[8];
+                uint32_t pk[TILE / 2];
+                auto exp_tile = [&](float m_use) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) sc[k] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < TILE / 2; ++j) {
+                        float x0, x1;
+                        ffma2_bc(s[2 * j], s[2 * j + 1], sl2, -m_use, x0, x1);
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        fadd2_acc(sc[2 * (j & 3)], sc[2 * (j & 3) + 1], p0, p1);
+                        pk[j] = pack_bf16(p0, p1);
+                    }
+                };
+                exp_tile(m_ref == -INFINITY ? 0.f : m_ref);
                 // row maximum: 8 independent chains of three-input maxima, then a tree
                 float mc[8];
 #pragma unroll
@@ -636,25 +658,12 @@ __global__ void __launch_bounds__(256, 1)
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool resc = m_new > m_ref + 8.0f;   // true when m_ref = -inf and m_new finite
                 float alpha = 1.f;
-                if (resc) {
-                    alpha = fast_exp2(m_ref - m_new);
-                    m_ref = m_new;
-                }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                // p = 2^(s * scale * log2(e) - m): arguments two lanes at a time, the
-                // running sums in four two-lane accumulators
-                float sc[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) sc[k] = 0.f;
-                uint32_t pk[TILE / 2];
-#pragma unroll
-                for (int j = 0; j < TILE / 2; ++j) {
-                    float x0, x1;
-                    ffma2_bc(s[2 * j], s[2 * j + 1], sl2, -m_use, x0, x1);
-                    const float p0 = fast_exp2(x0);
-                    const float p1 = fast_exp2(x1);
-                    fadd2_acc(sc[2 * (j & 3)], sc[2 * (j & 3) + 1], p0, p1);
-                    pk[j] = pack_bf16(p0, p1);
+                if (__any_sync(0xffffffffu, resc)) {
+                    if (resc) {
+                        alpha = fast_exp2(m_ref - m_new);
+                        m_ref = m_new;
+                    }
+                    exp_tile(m_ref == -INFINITY ? 0.f : m_ref);   // rows that kept m repeat the same values
                 }
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;

@@ -71,6 +71,10 @@ def _load():
         lib.oracle_attention.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                          vp, i64, vp, i64, ctypes.c_int, f64, vp, i64, vp, vp,
                                          ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                             vp, i64, vp, i64, ctypes.c_int, f64, vp, vp, vp, vp, vp,
+                                             ctypes.c_int]
         lib.oracle_rope.restype = ctypes.c_int
         lib.oracle_rope.argtypes = [vp, i64, i64, i64, vp, f64, ctypes.c_int, vp, vp]
         lib.oracle_round_bf16.restype = ctypes.c_float
@@ -140,6 +144,39 @@ def attention(q, k, v, *, causal=False, kpm=None, am=None, scale=None, q_pos0=0,
     if rows is None:
         return out.reshape(B, H, L, d), lse.reshape(B, H, L)
     return out, lse
+
+
+def attention_bwd(q, k, v, dout, *, causal=False, kpm=None, am=None, scale=None, q_pos0=0, k_pos0=0,
+                  nthreads=None):
+    """fp64 gradients of attention(q, k, v) contracted with dout (same shape as out).
+
+    Masks and positions as for attention().  Returns (dq, dk, dv, out, lse) as
+    float64 arrays of shapes (B,H,L,d), (B,H,S,d), (B,H,S,d), (B,H,L,d), (B,H,L).
+    """
+    lib = _load()
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, L, d = q.shape
+    S = k.shape[2]
+    assert k.shape == (B, H, S, d) and v.shape == (B, H, S, d) and dout.shape == q.shape
+    kpm, am = _u8(kpm), _u8(am)
+    if kpm is not None and (kpm.shape[0] < B or kpm.shape[1] < k_pos0 + S):
+        raise ValueError("key_padding_mask does not cover the key positions")
+    if am is not None and (am.shape[0] < q_pos0 + L or am.shape[1] < k_pos0 + S):
+        raise ValueError("attn_mask does not cover the (query, key) positions")
+    dq = np.zeros((B, H, L, d), dtype=np.float64)
+    dk = np.zeros((B, H, S, d), dtype=np.float64)
+    dv = np.zeros((B, H, S, d), dtype=np.float64)
+    out = np.zeros((B, H, L, d), dtype=np.float64)
+    lse = np.zeros((B, H, L), dtype=np.float64)
+    rc = lib.oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, L, S, d, q_pos0, k_pos0,
+                                  _ptr(kpm), 0 if kpm is None else kpm.shape[1],
+                                  _ptr(am), 0 if am is None else am.shape[1],
+                                  int(bool(causal)), 0.0 if scale is None else float(scale),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(out), _ptr(lse),
+                                  nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd: bad arguments")
+    return dq, dk, dv, out, lse
 
 
 def rope(x, base=10000.0, positions=None, round_to="bf16"):

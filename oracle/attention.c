@@ -213,3 +213,139 @@ int oracle_rope(const float *x, int64_t BH, int64_t T, int64_t d,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* attention backward                                                 */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Gradients of the attention of the section above with respect to q, k and v,
+ * contracted with dout: the plain chain rule through O_i = sum_j p_ij v_j,
+ * p_ij = exp(s_ij - LSE_i), s_ij = scale q_i . k_j over the visible j.  With
+ * D_i = dout_i . O_i ("Sequence/context parallelism" (brunomaga), section
+ * "Ring Attention", backward pass: the per-block gradients use the saved out
+ * and LSE of the whole row):
+ *   dV_j += p_ij dout_i,   dp_ij = dout_i . v_j,   ds_ij = p_ij (dp_ij - D_i),
+ *   dQ_i  = scale sum_j ds_ij k_j,   dK_j += scale ds_ij q_i.
+ * One thread takes whole (b, h) pairs, row after row, so dK and dV of a head
+ * are summed by one thread in row order.
+ */
+typedef struct {
+    attn_job a;                       /* geometry, masks, scale (rows unused) */
+    const float *dout;                /* (B,H,L,d) */
+    double *dq, *dk, *dv;             /* (B,H,L,d), (B,H,S,d), (B,H,S,d), zero on entry */
+    int64_t bh_begin, bh_end;
+} bwd_job;
+
+static void *bwd_worker(void *arg) {
+    const bwd_job *W = (const bwd_job *)arg;
+    const attn_job *J = &W->a;
+    const int64_t L = J->L, S = J->S, d = J->d;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    unsigned char *vis = (unsigned char *)malloc((size_t)(S > 0 ? S : 1));
+    for (int64_t bh = W->bh_begin; bh < W->bh_end; ++bh) {
+        const int64_t b = bh / J->H;
+        const float *kb = J->k + bh * S * d;
+        const float *vb = J->v + bh * S * d;
+        double *dkb = W->dk + bh * S * d;
+        double *dvb = W->dv + bh * S * d;
+        for (int64_t i = 0; i < L; ++i) {
+            const int64_t row = bh * L + i;
+            const float *qi = J->q + row * d;
+            const float *gi = W->dout + row * d;
+            double *dqi = W->dq + row * d;
+            double m = -INFINITY;
+            int64_t nvis = 0;
+            for (int64_t j = 0; j < S; ++j) {
+                vis[j] = (unsigned char)visible(J, b, i, j);
+                if (!vis[j]) continue;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += (double)qi[c] * (double)kb[j * d + c];
+                s[j] = dot * J->scale;
+                if (s[j] > m) m = s[j];
+                ++nvis;
+            }
+            J->lse[row] = -INFINITY;
+            for (int64_t c = 0; c < d; ++c) J->out[row * d + c] = 0.0;
+            if (nvis == 0) continue;   /* no visible key: out = 0 and every gradient of the row is 0 */
+            double sum = 0.0;
+            for (int64_t j = 0; j < S; ++j)
+                if (vis[j]) sum += exp(s[j] - m);
+            const double lse = m + log(sum);
+            J->lse[row] = lse;
+            for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+            for (int64_t j = 0; j < S; ++j) {
+                if (!vis[j]) continue;
+                p[j] = exp(s[j] - lse);
+                for (int64_t c = 0; c < d; ++c) o[c] += p[j] * (double)vb[j * d + c];
+            }
+            double D = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                J->out[row * d + c] = o[c];
+                D += (double)gi[c] * o[c];
+            }
+            for (int64_t j = 0; j < S; ++j) {
+                if (!vis[j]) continue;
+                double dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) dp += (double)gi[c] * (double)vb[j * d + c];
+                const double ds = p[j] * (dp - D);
+                for (int64_t c = 0; c < d; ++c) {
+                    dvb[j * d + c] += p[j] * (double)gi[c];
+                    dqi[c] += J->scale * ds * (double)kb[j * d + c];
+                    dkb[j * d + c] += J->scale * ds * (double)qi[c];
+                }
+            }
+        }
+    }
+    free(s);
+    free(p);
+    free(o);
+    free(vis);
+    return NULL;
+}
+
+/*
+ * Exact (fp64) attention gradients.  dq, dk, dv, out, lse are written in full
+ * (out and lse are the forward values of the same call).  Returns 0, or -1 on
+ * a bad argument.
+ */
+int oracle_attention_bwd(const float *q, const float *k, const float *v, const float *dout,
+                         int64_t B, int64_t H, int64_t L, int64_t S, int64_t d,
+                         int64_t q_pos0, int64_t k_pos0,
+                         const uint8_t *kpm, int64_t kpm_ld,
+                         const uint8_t *am, int64_t am_ld,
+                         int causal, double scale,
+                         double *dq, double *dk, double *dv, double *out, double *lse, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !out || !lse) return -1;
+    if (B < 0 || H < 0 || L < 0 || S < 0 || d <= 0) return -1;
+    const int64_t BH = B * H;
+    memset(dq, 0, sizeof(double) * (size_t)(BH * L * d));
+    memset(dk, 0, sizeof(double) * (size_t)(BH * S * d));
+    memset(dv, 0, sizeof(double) * (size_t)(BH * S * d));
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (BH < nthreads) nthreads = BH > 0 ? (int)BH : 1;
+    bwd_job base;
+    memset(&base, 0, sizeof base);
+    base.a.q = q; base.a.k = k; base.a.v = v;
+    base.a.B = B; base.a.H = H; base.a.L = L; base.a.S = S; base.a.d = d;
+    base.a.q_pos0 = q_pos0; base.a.k_pos0 = k_pos0;
+    base.a.kpm = kpm; base.a.kpm_ld = kpm_ld; base.a.am = am; base.a.am_ld = am_ld;
+    base.a.causal = causal; base.a.scale = scale > 0 ? scale : 1.0 / sqrt((double)d);
+    base.a.out = out; base.a.lse = lse;
+    base.dout = dout; base.dq = dq; base.dk = dk; base.dv = dv;
+    bwd_job *jobs = (bwd_job *)malloc(sizeof(bwd_job) * (size_t)nthreads);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].bh_begin = BH * t / nthreads;
+        jobs[t].bh_end = BH * (t + 1) / nthreads;
+        pthread_create(&th[t], NULL, bwd_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+    return 0;
+}

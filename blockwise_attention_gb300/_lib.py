@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "libblockattn.so")
-_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu"]
+_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu"]
 _HEADERS = ["common.cuh", "internal.h", "epilogue.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -95,7 +95,8 @@ class ba_tensor(ctypes.Structure):
 
 EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ring_attn_fwd",
             "ring_attn_fwd_workspace_size", "rope_apply", "ba_tile_classes", "ba_index_maps",
-            "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc"]
+            "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc",
+            "attn_block_bwd", "attn_block_bwd_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size"]
 
 
 def load(path: str | None = None):
@@ -135,6 +136,16 @@ def load(path: str | None = None):
     lib.ba_sync_status.argtypes = [vp]
     lib.ba_debug_wait_timeout.restype = i
     lib.ba_debug_wait_timeout.argtypes = [i64, vp]
+    lib.attn_block_bwd_workspace_size.restype = sz
+    lib.attn_block_bwd_workspace_size.argtypes = [i, i, i]
+    lib.attn_block_bwd.restype = i
+    lib.attn_block_bwd.argtypes = [T, T, T, T, T, vp, i, i, i, i, i, i, i64, i64, vp, i64, vp, i64, i, f,
+                                   vp, vp, vp, i, vp, sz, vp]
+    lib.ring_attn_bwd_workspace_size.restype = sz
+    lib.ring_attn_bwd_workspace_size.argtypes = [i, i, i]
+    lib.ring_attn_bwd.restype = i
+    lib.ring_attn_bwd.argtypes = [T, T, T, T, T, vp, i, i, i, i, i, i, i, i, vp, i64, vp, i64, i, f,
+                                  vp, vp, vp, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -293,6 +304,74 @@ def ring_attn_fwd(q, k, v, *, P, partition="contiguous", mode="fused", key_paddi
         arr = np.ctypeslib.as_array(maps).copy()
         return out, lse, arr[:T].reshape(P, T // P), arr[T:].reshape(P, P)
     return out, lse
+
+
+def _grads(B, H, Lq, Lk, d, device, dq, dk, dv):
+    shapes = ((dq, (B, H, Lq, d)), (dk, (B, H, Lk, d)), (dv, (B, H, Lk, d)))
+    res = []
+    for t, shape in shapes:
+        if t is None:
+            t = torch.empty(shape, dtype=torch.float32, device=device)
+        elif t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape or not t.is_cuda:
+            raise ValueError(f"gradient buffers must be contiguous fp32 CUDA tensors of shape {shape}")
+        res.append(t)
+    return res
+
+
+def _check_bwd_inputs(q, out, dout, lse):
+    if out.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("out and dout must have the dtype of q")
+    if out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("out and dout must have the shape of q")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (B, H, L)")
+
+
+def attn_block_bwd(q, k, v, out, dout, lse, *, q_off=0, k_off=0, key_padding_mask=None, attn_mask=None,
+                   causal=False, scale=None, dq=None, dk=None, dv=None, accumulate=False, workspace=None,
+                   stream=None):
+    """Gradients (dq, dk, dv) (fp32) of one attention block given the forward
+    out and lse of the whole rows; see include/blockattn.h."""
+    lib = load()
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    _check_bwd_inputs(q, out, dout, lse)
+    dq, dk, dv = _grads(B, H, Lq, Lk, d, q.device, dq, dk, dv)
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    need = lib.attn_block_bwd_workspace_size(B, H, Lq)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib.attn_block_bwd(_tensor(q), _tensor(k), _tensor(v), _tensor(out), _tensor(dout), _ptr(lse), B, H, Lq,
+                            Lk, d, _dtype_code(q.dtype), q_off, k_off, kpm, kpm_ld, am, am_ld, int(bool(causal)),
+                            0.0 if scale is None else float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                            int(bool(accumulate)), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                            _stream(stream))
+    _check("attn_block_bwd", rc)
+    return dq, dk, dv
+
+
+def ring_attn_bwd(q, k, v, out, dout, lse, *, P, partition="contiguous", mode="fused", key_padding_mask=None,
+                  attn_mask=None, causal=False, scale=None, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """Ring Attention backward over P emulated ranks: (dq, dk, dv) fp32 in global
+    token order; see include/blockattn.h."""
+    lib = load()
+    B, H, T, d = q.shape
+    _check_bwd_inputs(q, out, dout, lse)
+    dq, dk, dv = _grads(B, H, T, T, d, q.device, dq, dk, dv)
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    need = lib.ring_attn_bwd_workspace_size(B, H, T)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib.ring_attn_bwd(_tensor(q), _tensor(k), _tensor(v), _tensor(out), _tensor(dout), _ptr(lse), B, H, T, d,
+                           _dtype_code(q.dtype), P, PARTITIONS[partition], MODES[mode], kpm, kpm_ld, am, am_ld,
+                           int(bool(causal)), 0.0 if scale is None else float(scale), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                           _stream(stream))
+    _check("ring_attn_bwd", rc)
+    return dq, dk, dv
 
 
 def rope_apply(x, *, x2=None, base=10000.0, positions=None, out=None, out2=None, stream=None):

@@ -852,6 +852,144 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     return BA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Backward
+// ---------------------------------------------------------------------------
+
+namespace {
+
+ba::TensorRef tref(const ba_tensor &t) { return ba::TensorRef{t.ptr, t.sB, t.sH, t.sT}; }
+
+int check_bwd_common(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout, const float *lse,
+                     int B, int H, int Lq, int Lk, int d, int dtype, const float *dq, const float *dk,
+                     const float *dv) {
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    const bool qrows = (long long)B * H * Lq > 0, krows = (long long)B * H * Lk > 0;
+    if (qrows && (check_tensor(q) || check_tensor(out) || check_tensor(dout) || !lse || !dq)) return BA_ERR_ARG;
+    if (krows && (check_tensor(k) || check_tensor(v) || !dk || !dv)) return BA_ERR_ARG;
+    return BA_OK;
+}
+
+}  // namespace
+
+size_t attn_block_bwd_workspace_size(int B, int H, int Lq) {
+    if (B < 0 || H < 0 || Lq < 0) return 0;
+    return align256((size_t)4 * (size_t)B * (size_t)H * (size_t)Lq);
+}
+
+int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout, const float *lse, int B,
+                   int H, int Lq, int Lk, int d, int dtype, int64_t q_off, int64_t k_off,
+                   const uint8_t *key_padding_mask, int64_t kpm_ld, const uint8_t *attn_mask, int64_t am_ld,
+                   int causal, float scale, float *dq, float *dk, float *dv, int accumulate, void *workspace,
+                   size_t workspace_bytes, ba_stream_t stream) {
+    int rc = check_bwd_common(q, k, v, out, dout, lse, B, H, Lq, Lk, d, dtype, dq, dk, dv);
+    if (rc) return rc;
+    if (q_off < 0 || k_off < 0) return BA_ERR_ARG;
+    if ((key_padding_mask && kpm_ld < k_off + Lk) || (attn_mask && am_ld < k_off + Lk)) return BA_ERR_ARG;
+    if (B == 0 || H == 0 || (Lq == 0 && Lk == 0)) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    if ((rc = device_setup(dev))) return rc;
+    Scratch ws;
+    if ((rc = ws.acquire(workspace, workspace_bytes, attn_block_bwd_workspace_size(B, H, Lq), stream))) return rc;
+    ba::BwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.B = B;
+    a.H = H;
+    a.d = d;
+    a.dtype = dtype;
+    a.ring = 0;
+    a.Lq = Lq;
+    a.Lk = Lk;
+    a.q_off = q_off;
+    a.k_off = k_off;
+    a.causal = causal != 0;
+    a.kpm = key_padding_mask;
+    a.kpm_ld = kpm_ld;
+    a.am = attn_mask;
+    a.am_ld = am_ld;
+    a.q = tref(fix_unit_strides(q, B, H, Lq, d));
+    a.out = tref(fix_unit_strides(out, B, H, Lq, d));
+    a.dout = tref(fix_unit_strides(dout, B, H, Lq, d));
+    a.k = tref(fix_unit_strides(k, B, H, Lk, d));
+    a.v = tref(fix_unit_strides(v, B, H, Lk, d));
+    a.lse = lse;
+    a.D = static_cast<float *>(ws.ptr);
+    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.accumulate = accumulate != 0;
+    return ba::launch_attn_bwd(a, g_num_sms[dev], stream);
+}
+
+size_t ring_attn_bwd_workspace_size(int B, int H, int T) { return attn_block_bwd_workspace_size(B, H, T); }
+
+int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout, const float *lse, int B,
+                  int H, int T, int d, int dtype, int P, int partition, int mode, const uint8_t *key_padding_mask,
+                  int64_t kpm_ld, const uint8_t *attn_mask, int64_t am_ld, int causal, float scale, float *dq,
+                  float *dk, float *dv, void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+    int rc = check_bwd_common(q, k, v, out, dout, lse, B, H, T, T, d, dtype, dq, dk, dv);
+    if (rc) return rc;
+    if (P < 1) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    if (mode != BA_MODE_STEPWISE && mode != BA_MODE_FUSED) return BA_ERR_ARG;
+    if ((key_padding_mask && kpm_ld < T) || (attn_mask && am_ld < T)) return BA_ERR_ARG;
+    const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
+    if (T % NC) return BA_ERR_SHAPE;
+    if (B == 0 || H == 0 || T == 0) return BA_OK;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    if ((rc = device_setup(dev))) return rc;
+    Scratch ws;
+    if ((rc = ws.acquire(workspace, workspace_bytes, ring_attn_bwd_workspace_size(B, H, T), stream))) return rc;
+    ba::BwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.B = B;
+    a.H = H;
+    a.d = d;
+    a.dtype = dtype;
+    a.ring = 1;
+    a.T = T;
+    a.P = P;
+    a.zigzag = partition == BA_PART_ZIGZAG;
+    a.NC = NC;
+    a.CL = T / NC;
+    a.causal = causal != 0;
+    a.kpm = key_padding_mask;
+    a.kpm_ld = kpm_ld;
+    a.am = attn_mask;
+    a.am_ld = am_ld;
+    a.q = tref(fix_unit_strides(q, B, H, T, d));
+    a.out = tref(fix_unit_strides(out, B, H, T, d));
+    a.dout = tref(fix_unit_strides(dout, B, H, T, d));
+    a.k = tref(fix_unit_strides(k, B, H, T, d));
+    a.v = tref(fix_unit_strides(v, B, H, T, d));
+    a.lse = lse;
+    a.D = static_cast<float *>(ws.ptr);
+    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    if (mode == BA_MODE_FUSED || P == 1) {
+        a.s_begin = 0;
+        a.s_end = P;
+        a.accumulate = 0;
+        return ba::launch_attn_bwd(a, g_num_sms[dev], stream);
+    }
+    // Step-wise, as on the page: step s pairs the queries of rank r with the
+    // K/V block of rank (r - s) mod P; dQ accumulates in place and dK / dV
+    // accumulate at their block's rows (the page rotates them with K and V).
+    for (int s = 0; s < P; ++s) {
+        a.s_begin = s;
+        a.s_end = s + 1;
+        a.accumulate = s > 0;
+        if ((rc = ba::launch_attn_bwd(a, g_num_sms[dev], stream))) return rc;
+    }
+    return BA_OK;
+}
+
 // Same work as attn_block_fwd, with the tile-class map in the library's fixed
 // device array instead of a workspace: nothing is allocated.
 int attn_block_fwd_noalloc(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,

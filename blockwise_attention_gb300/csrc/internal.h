@@ -29,6 +29,36 @@ struct AttnArgs {
     unsigned long long wait_limit_ns;    // bounded-wait limit
 };
 
+// A (B, H, rows, d) tensor with element strides, d contiguous.
+struct TensorRef {
+    const void *p;
+    long long sB, sH, sT;
+};
+
+// Arguments of the attention backward (block or ring geometry).  Rows of
+// q/out/dout and of k/v are positions - off in block mode and token positions
+// in ring mode (global token order).
+struct BwdArgs {
+    int B, H, d, dtype;
+    int ring;                            // 0: one block (Lq x Lk at q_off / k_off)
+    int Lq, Lk;
+    long long q_off, k_off;
+    int T, P, zigzag, CL, NC, s_begin, s_end;   // ring geometry and the steps to cover
+    int causal;
+    const uint8_t *kpm;
+    long long kpm_ld;
+    const uint8_t *am;
+    long long am_ld;
+    TensorRef q, k, v, out, dout;
+    const float *lse;                    // (B, H, Lq) natural-log LSE of the whole row
+    float *D;                            // (B, H, Lq) dout . out, written by the pre-pass
+    float scale;
+    float *dq, *dk, *dv;                 // fp32 (B, H, L, d) contiguous
+    int accumulate;                      // add into dq / dk / dv instead of overwriting
+};
+
+int launch_attn_bwd(const BwdArgs &a, int num_sms, cudaStream_t s);
+
 // TMA descriptors of Q, K, V for the tensor-core kernel.
 struct TmaMaps {
     CUtensorMap q, k, v;

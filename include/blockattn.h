@@ -160,6 +160,65 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v,
                   void *workspace, size_t workspace_bytes, ba_stream_t stream);
 
 /*
+ * attn_block_bwd -- gradients of one attention block ("Sequence/context
+ * parallelism" (brunomaga), section "Ring Attention", backward pass): with
+ * p_ij = exp(scale q_i . k_j - lse_i) over the visible pairs and
+ * D_i = dout_i . out_i,
+ *   dV_j = sum_i p_ij dout_i,   ds_ij = p_ij (dout_i . v_j - D_i),
+ *   dQ_i = scale sum_j ds_ij k_j,   dK_j = scale sum_i ds_ij q_i.
+ * out and lse are the forward results of the WHOLE rows (all keys, not just
+ * this block), as the page's per-step backward uses them; the blocks' dQ, dK,
+ * dV then add up to the gradients of the full attention.
+ *  q, out, dout: (B, H, Lq, d); k, v: (B, H, Lk, d); strides and dtype as
+ *    for attn_block_fwd (q, k, v, out, dout share the dtype).
+ *  lse: (B, H, Lq) fp32 natural log, -inf for rows that see no key.
+ *  q_off, k_off, masks, causal, scale: as for attn_block_fwd.
+ *  dq: (B, H, Lq, d), dk, dv: (B, H, Lk, d), fp32 contiguous, caller-owned.
+ *  accumulate: 0 = overwrite dq, dk, dv; 1 = add this block's gradients.
+ *  workspace: attn_block_bwd_workspace_size() bytes (the D_i vector).
+ * Runs on the CUDA cores in fp32 (no tensor-core backward yet).
+ * Errors: BA_ERR_ARG (NULL pointers for non-empty sides, negative sizes or
+ * offsets, masks not covering the global positions), BA_ERR_SHAPE (d not in
+ * {16, 32, 64, 128}).
+ */
+size_t attn_block_bwd_workspace_size(int B, int H, int Lq);
+int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout,
+                   const float *lse, int B, int H, int Lq, int Lk, int d, int dtype,
+                   int64_t q_off, int64_t k_off,
+                   const uint8_t *key_padding_mask, int64_t kpm_ld,
+                   const uint8_t *attn_mask, int64_t am_ld,
+                   int causal, float scale,
+                   float *dq, float *dk, float *dv, int accumulate,
+                   void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
+ * ring_attn_bwd -- the backward pass of Ring Attention over P emulated ranks
+ * ("Sequence/context parallelism" (brunomaga), section "Ring Attention",
+ * backward): at step s rank r pairs its queries with the K/V block of rank
+ * (r - s) mod P; dQ accumulates at the queries, and dK / dV accumulate with
+ * their K/V block (the page rotates them around the ring with K and V, so
+ * after P steps each rank holds the gradients of its own block).  On one GPU
+ * the ranks are the token ranges of the partition, so a block's dK / dV rows
+ * collect the contributions of every rank's queries in place.
+ *  q, k, v, out, dout: (B, H, T, d) in global token order; lse: (B, H, T).
+ *  mode: BA_MODE_FUSED = every step in one launch pair; BA_MODE_STEPWISE =
+ *    one launch pair per ring step, accumulating, as on the page.
+ *  dq, dk, dv: (B, H, T, d) fp32 contiguous, overwritten.
+ *  workspace: ring_attn_bwd_workspace_size() bytes.
+ * Errors: as attn_block_bwd, plus BA_ERR_SHAPE when T is not divisible by P
+ * (contiguous) or 2P (zigzag).
+ */
+size_t ring_attn_bwd_workspace_size(int B, int H, int T);
+int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout,
+                  const float *lse, int B, int H, int T, int d, int dtype,
+                  int P, int partition, int mode,
+                  const uint8_t *key_padding_mask, int64_t kpm_ld,
+                  const uint8_t *attn_mask, int64_t am_ld,
+                  int causal, float scale,
+                  float *dq, float *dk, float *dv,
+                  void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
  * rope_apply -- rotary position embedding ("RoFormer", item #4 of ai.engineer
  * "Transformers and Attention"): split each d-vector into coordinate pairs
  * (2c, 2c+1) and rotate pair c by the angle m * base^(-2c/d), m the token

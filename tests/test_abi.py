@@ -75,6 +75,15 @@ def test_argument_errors_are_host_side():
     # ring: odd d with rope
     assert lib.rope_apply(T1, T0, 1, 1, 8, 7, 1, None, 1e4, dummy, None, None) == _lib.BA_ERR_ARG
     assert lib.attn_merge(None, dummy, dummy, dummy, 4, 4, None) == _lib.BA_ERR_ARG
+    # backward: NULL out, unsupported d, T not divisible by 2P, masks not covering positions
+    assert lib.attn_block_bwd(T1, T1, T1, T0, T1, dummy, 1, 1, 8, 8, 64, 1, 0, 0, None, 0, None, 0, 0, 0.0,
+                              dummy, dummy, dummy, 0, None, 0, None) == _lib.BA_ERR_ARG
+    assert lib.attn_block_bwd(T1, T1, T1, T1, T1, dummy, 1, 1, 8, 8, 48, 1, 0, 0, None, 0, None, 0, 0, 0.0,
+                              dummy, dummy, dummy, 0, None, 0, None) == _lib.BA_ERR_SHAPE
+    assert lib.attn_block_bwd(T1, T1, T1, T1, T1, dummy, 1, 1, 8, 8, 64, 1, 0, 4, dummy, 8, None, 0, 0, 0.0,
+                              dummy, dummy, dummy, 0, None, 0, None) == _lib.BA_ERR_ARG
+    assert lib.ring_attn_bwd(T1, T1, T1, T1, T1, dummy, 1, 1, 12, 64, 1, 4, 1, 1, None, 0, None, 0, 1, 0.0,
+                             dummy, dummy, dummy, None, 0, None) == _lib.BA_ERR_SHAPE
 
 
 def test_workspace_sizes():

@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
+                    help="backward: time ring_attn_bwd instead (not the default bench line)")
     return ap.parse_args()
 
 
@@ -419,6 +421,99 @@ def native_arm(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "attention backward TFLOP/s (10*d FLOP per visible pair: QK^T, dout V^T, dV, dK, dQ)"
+
+
+def backward_arm(args, w, rank, world, local_rank):
+    """Time ring_attn_bwd (fused) on the workload; out and lse come from one
+    forward before the timed region.  The kernels run on the CUDA cores in fp32,
+    so the roofline is the fp32 FMA peak (152 SMs x 128 lanes x 2 FLOP x clock)."""
+    import blockwise_attention_gb300 as ba
+    from blockwise_attention_gb300.workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    inp = make_inputs(w, dev)
+    if w.rope_base is not None:
+        q, k = ba.rope_apply(inp.q, x2=inp.k, base=w.rope_base)
+    else:
+        q, k = inp.q, inp.k
+    out, lse = ba.ring_attn_fwd(q, k, inp.v, P=w.P, partition=w.partition, key_padding_mask=inp.kpm,
+                                attn_mask=inp.am, causal=w.causal)
+    g = torch.Generator(device="cpu").manual_seed(2000 + w.index)
+    dout = torch.randn(inp.q.shape, generator=g).to(inp.q.dtype).to(dev)
+    dq = torch.empty(inp.q.shape, dtype=torch.float32, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+    need = ba.load().ring_attn_bwd_workspace_size(w.B, w.H, w.T)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    pairs = visible_pairs(w, inp)
+    flops = 10.0 * w.d * pairs
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ba.ring_attn_bwd(q, k, inp.v, out, dout, lse, P=w.P, partition=w.partition, mode=args.mode,
+                         key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, dq=dq, dk=dk, dv=dv,
+                         workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ba.sync_status() != 0:
+        raise RuntimeError("device status error after warm-up")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+    if rank != 0:
+        return
+    value = world * flops / (ms * 1e-3) / 1e12
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    steps_per = 1 if args.mode == "fused" else w.P
+    cpu = None
+    if not args.no_cpu:
+        import oracle
+        oracle.build()
+        n = min(w.T, 2048)
+        sl = (slice(0, 1), slice(0, 1), slice(0, n))
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q[sl].float().cpu(), k[sl].float().cpu(), inp.v[sl].float().cpu(),
+                             dout[sl].float().cpu(), causal=w.causal)
+        dt = time.perf_counter() - t0
+        cpairs = n * (n + 1) // 2 if w.causal else n * n
+        cpu = {"value": 10.0 * w.d * cpairs / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"backward of the first {n} tokens of one head (b=0, h=0) of {w.name}, "
+                         f"{cpairs} visible pairs in {dt:.2f} s (one thread per head)"}
+    line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": w.P,
+                       "partition": w.partition, "causal": w.causal, "mode": args.mode, "direction": "backward",
+                       "visible_pairs": pairs, "flops_per_step": flops,
+                       "l2": "inputs larger than the 129 MB L2; no flush"},
+            "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                         "frac": value / peak, "traffic": None, "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x sampled SM clock; the "
+                                        "kernels execute 14*d FLOP per pair (scores and dout V^T in both)"},
+            "cpu_baseline": cpu, "e2e": None, "clocks": clocks,
+            "gpu_launches": 3 * steps_per * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from blockwise_attention_gb300.workloads import WORKLOADS
@@ -432,7 +527,10 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     try:
-        native_arm(args, w, rank, world, local_rank)
+        if args.direction == "backward":
+            backward_arm(args, w, rank, world, local_rank)
+        else:
+            native_arm(args, w, rank, world, local_rank)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

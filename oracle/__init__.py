@@ -179,6 +179,38 @@ def attention_bwd(q, k, v, dout, *, causal=False, kpm=None, am=None, scale=None,
     return dq, dk, dv, out, lse
 
 
+def ulysses_token_to_head(x_tok: np.ndarray, P: int) -> np.ndarray:
+    """The first Ulysses all-to-all ("Sequence/context parallelism" (brunomaga),
+    section "Ulysses sequence parallelism"; "Change token partitions into head
+    partitions with Ulysses"): rank r holds tokens [r T/P, (r+1) T/P) of every
+    head, as x_tok[r] of shape (H, B, T/P, d); afterwards rank r holds heads
+    [r H/P, (r+1) H/P) for all T tokens, as (H/P, B, T, d).  Written as the
+    exchange itself: rank r receives, from every rank s, s's tokens of r's heads,
+    and places them at s's token range."""
+    P_, H, B, Tl, d = x_tok.shape
+    assert P_ == P and H % P == 0
+    hl = H // P
+    out = np.empty((P, hl, B, Tl * P, d), dtype=x_tok.dtype)
+    for r in range(P):          # receiving rank
+        for s in range(P):      # sending rank
+            out[r, :, :, s * Tl:(s + 1) * Tl, :] = x_tok[s, r * hl:(r + 1) * hl, :, :, :]
+    return out
+
+
+def ulysses_head_to_token(x_head: np.ndarray, P: int) -> np.ndarray:
+    """The second (reverse) Ulysses all-to-all: rank r holds heads
+    [r H/P, (r+1) H/P) for all T tokens, as (H/P, B, T, d); afterwards rank r
+    holds tokens [r T/P, (r+1) T/P) of every head, as (H, B, T/P, d)."""
+    P_, hl, B, T, d = x_head.shape
+    assert P_ == P and T % P == 0
+    Tl = T // P
+    out = np.empty((P, hl * P, B, Tl, d), dtype=x_head.dtype)
+    for r in range(P):          # receiving rank (token range)
+        for s in range(P):      # sending rank (head range)
+            out[r, s * hl:(s + 1) * hl, :, :, :] = x_head[s, :, :, r * Tl:(r + 1) * Tl, :]
+    return out
+
+
 def rope(x, base=10000.0, positions=None, round_to="bf16"):
     """Rotate coordinate pairs of x (..., T, d).  round_to: "bf16", "f32" or None
     (None returns the unrounded float64 rotation)."""

@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses"],
+                    help="ulysses: time ulysses_attn_fwd over P head-partitioned ranks (not the default line)")
     ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
                     help="backward: time ring_attn_bwd instead (not the default bench line)")
     return ap.parse_args()
@@ -514,6 +516,84 @@ def backward_arm(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def ulysses_arm(args, w, rank, world, local_rank):
+    """Time ulysses_attn_fwd on token shards (P, H, B, T/P, d): three exchanges,
+    one attention launch, and the reverse exchange of out and lse.  `value` is
+    attention TFLOP/s over visible pairs for the whole step; `roofline` is the
+    exchange kernel against the measured HBM copy peak (it reads and writes each
+    byte once)."""
+    import blockwise_attention_gb300 as ba
+    from blockwise_attention_gb300.workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    inp = make_inputs(w, dev)
+    P = w.P
+    if w.H % P:
+        raise SystemExit(f"ulysses needs P | H ({w.name}: H={w.H}, P={P})")
+
+    def to_tok(x):
+        B, H, T, d = x.shape
+        return x.permute(1, 0, 2, 3).reshape(H, B, P, T // P, d).permute(2, 0, 1, 3, 4).contiguous()
+
+    qt, kt, vt = to_tok(inp.q), to_tok(inp.k), to_tok(inp.v)
+    out = torch.empty_like(qt)
+    lse = torch.empty(qt.shape[:4], dtype=torch.float32, device=dev)
+    need = ba.load().ulysses_attn_fwd_workspace_size(P, w.H, w.B, w.T, w.d, 1 if w.torch_dtype == torch.bfloat16
+                                                      else 0, int(inp.kpm is not None or inp.am is not None))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    head = torch.empty((P, w.H // P, w.B, w.T, w.d), dtype=qt.dtype, device=dev)
+    pairs = visible_pairs(w, inp)
+    flops = 4.0 * w.d * pairs
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ba.ulysses_attn_fwd(qt, kt, vt, key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, out=out,
+                            lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+        ba.ulysses_all_to_all(qt, P, "token_to_head", out=head)
+    torch.cuda.synchronize()
+    if ba.sync_status() != 0:
+        raise RuntimeError("device status error after warm-up")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    for _ in range(args.steps):
+        ba.ulysses_all_to_all(qt, P, "token_to_head", out=head)
+    c.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+    a2a_ms = b.elapsed_time(c) / args.steps
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    a2a_bytes = 2.0 * qt.numel() * qt.element_size()
+    achieved = a2a_bytes / (a2a_ms * 1e-3) / 1e9
+    value = world * flops / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if qt.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "variant": "ulysses", "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": P,
+                       "causal": w.causal, "visible_pairs": pairs, "flops_per_step": flops,
+                       "l2": "inputs larger than the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "a2a_kernel (token->head)",
+                         "algorithmic_bytes": a2a_bytes, "kernel_ms": a2a_ms,
+                         "peak_source": f"{src} hbm_gbs (copy)"},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": 7 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from blockwise_attention_gb300.workloads import WORKLOADS
@@ -529,6 +609,8 @@ def main():
     try:
         if args.direction == "backward":
             backward_arm(args, w, rank, world, local_rank)
+        elif args.variant == "ulysses":
+            ulysses_arm(args, w, rank, world, local_rank)
         else:
             native_arm(args, w, rank, world, local_rank)
     finally:

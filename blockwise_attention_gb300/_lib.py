@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "libblockattn.so")
-_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu"]
+_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu", "ulysses.cu"]
 _HEADERS = ["common.cuh", "internal.h", "epilogue.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -96,7 +96,8 @@ class ba_tensor(ctypes.Structure):
 EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ring_attn_fwd",
             "ring_attn_fwd_workspace_size", "rope_apply", "ba_tile_classes", "ba_index_maps",
             "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc",
-            "attn_block_bwd", "attn_block_bwd_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size"]
+            "attn_block_bwd", "attn_block_bwd_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
+            "ulysses_all_to_all", "ulysses_attn_fwd", "ulysses_attn_fwd_workspace_size"]
 
 
 def load(path: str | None = None):
@@ -146,6 +147,12 @@ def load(path: str | None = None):
     lib.ring_attn_bwd.restype = i
     lib.ring_attn_bwd.argtypes = [T, T, T, T, T, vp, i, i, i, i, i, i, i, i, vp, i64, vp, i64, i, f,
                                   vp, vp, vp, vp, sz, vp]
+    lib.ulysses_all_to_all.restype = i
+    lib.ulysses_all_to_all.argtypes = [vp, vp, i, i, i, i, i, i, i, vp]
+    lib.ulysses_attn_fwd_workspace_size.restype = sz
+    lib.ulysses_attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.ulysses_attn_fwd.restype = i
+    lib.ulysses_attn_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, i64, vp, i64, i, f, vp, vp, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -372,6 +379,67 @@ def ring_attn_bwd(q, k, v, out, dout, lse, *, P, partition="contiguous", mode="f
                            _stream(stream))
     _check("ring_attn_bwd", rc)
     return dq, dk, dv
+
+
+A2A = {"token_to_head": 0, "head_to_token": 1}
+
+
+def ulysses_all_to_all(x, P, direction, *, out=None, stream=None):
+    """One Ulysses exchange of a contiguous stacked array: token_to_head takes
+    (P, H, B, T/P, d) to (P, H/P, B, T, d); head_to_token is the inverse."""
+    lib = load()
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("ulysses_all_to_all takes a contiguous CUDA tensor")
+    if direction == "token_to_head":
+        P_, H, B, Tl, d = x.shape
+        shape, T = (P, H // P, B, Tl * P, d), Tl * P
+    elif direction == "head_to_token":
+        P_, hl, B, T, d = x.shape
+        H = hl * P
+        shape = (P, H, B, T // P, d)
+    else:
+        raise ValueError(direction)
+    if P_ != P:
+        raise ValueError("leading axis must be P")
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    elif tuple(out.shape) != shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous tensor of shape {shape}")
+    rc = lib.ulysses_all_to_all(_ptr(x), _ptr(out), P, H, B, T, d, x.element_size(), A2A[direction],
+                                _stream(stream))
+    _check("ulysses_all_to_all", rc)
+    return out
+
+
+def ulysses_attn_fwd(q_tok, k_tok, v_tok, *, key_padding_mask=None, attn_mask=None, causal=False, scale=None,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Ulysses attention over P emulated ranks from token shards (P, H, B, T/P, d):
+    returns (out (P, H, B, T/P, d), lse (P, H, B, T/P) fp32); see include/blockattn.h."""
+    lib = load()
+    for t in (q_tok, k_tok, v_tok):
+        if not t.is_contiguous() or not t.is_cuda or t.shape != q_tok.shape or t.dtype != q_tok.dtype:
+            raise ValueError("q_tok, k_tok, v_tok must be contiguous CUDA tensors of one shape and dtype")
+    P, H, B, Tl, d = q_tok.shape
+    T = P * Tl
+    if out is None:
+        out = torch.empty_like(q_tok)
+    if lse is None:
+        lse = torch.empty((P, H, B, Tl), dtype=torch.float32, device=q_tok.device)
+    if tuple(out.shape) != tuple(q_tok.shape) or out.dtype != q_tok.dtype or not out.is_contiguous():
+        raise ValueError("out must be contiguous, of the shape and dtype of q_tok")
+    if tuple(lse.shape) != (P, H, B, Tl) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape (P, H, B, T/P)")
+    kpm, kpm_ld = _mask(key_padding_mask)
+    am, am_ld = _mask(attn_mask)
+    dt = _dtype_code(q_tok.dtype)
+    need = lib.ulysses_attn_fwd_workspace_size(P, H, B, T, d, dt, int(kpm is not None or am is not None))
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_tok.device)
+    rc = lib.ulysses_attn_fwd(_ptr(q_tok), _ptr(k_tok), _ptr(v_tok), P, H, B, T, d, dt, kpm, kpm_ld, am, am_ld,
+                              int(bool(causal)), 0.0 if scale is None else float(scale), _ptr(out), _ptr(lse),
+                              _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("ulysses_attn_fwd", rc)
+    return out, lse
 
 
 def rope_apply(x, *, x2=None, base=10000.0, positions=None, out=None, out2=None, stream=None):

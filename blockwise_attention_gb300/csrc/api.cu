@@ -990,6 +990,108 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
     return BA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Ulysses
+// ---------------------------------------------------------------------------
+
+int ulysses_all_to_all(const void *src, void *dst, int P, int H, int B, int T, int d, int elem_bytes, int direction,
+                       ba_stream_t stream) {
+    if (P < 1 || H < 0 || B < 0 || T < 0 || d < 1) return BA_ERR_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return BA_ERR_ARG;
+    if (direction != BA_A2A_TOKEN_TO_HEAD && direction != BA_A2A_HEAD_TO_TOKEN) return BA_ERR_ARG;
+    if (H % P || T % P) return BA_ERR_SHAPE;
+    if ((long long)H * B * T == 0) return BA_OK;
+    if (!src || !dst) return BA_ERR_ARG;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    ba::UlyssesArgs u;
+    u.P = P;
+    u.H = H;
+    u.B = B;
+    u.Tl = T / P;
+    u.elem_bytes = elem_bytes;
+    u.row_bytes = (long long)d * elem_bytes;
+    // head side: the stacked (P, H/P, B, T, d) array, i.e. (B, H, T, d) with sH = B T d
+    u.sT = d;
+    u.sB = (long long)T * d;
+    u.sH = (long long)B * T * d;
+    u.to_head = direction == BA_A2A_TOKEN_TO_HEAD;
+    u.tok = u.to_head ? const_cast<void *>(src) : dst;
+    u.head = u.to_head ? dst : const_cast<void *>(src);
+    return ba::launch_ulysses_a2a(u, g_num_sms[dev], stream);
+}
+
+size_t ulysses_attn_fwd_workspace_size(int P, int H, int B, int T, int d, int dtype, int has_masks) {
+    if (P < 1 || H < 0 || B < 0 || T < 0 || d < 1 || !valid_dtype(dtype)) return 0;
+    const size_t tensor = (size_t)B * H * T * d * elem_size(dtype);
+    return 4 * align256(tensor) + align256((size_t)B * H * T * 4) +
+           ring_attn_fwd_workspace_size(B, H, T, d, dtype, 1, BA_PART_CONTIGUOUS, BA_MODE_FUSED, has_masks, 0, dtype);
+}
+
+int ulysses_attn_fwd(const void *q_tok, const void *k_tok, const void *v_tok, int P, int H, int B, int T, int d,
+                     int dtype, const uint8_t *key_padding_mask, int64_t kpm_ld, const uint8_t *attn_mask,
+                     int64_t am_ld, int causal, float scale, void *out_tok, float *lse_tok, void *workspace,
+                     size_t workspace_bytes, ba_stream_t stream) {
+    if (P < 1 || H < 0 || B < 0 || T < 0 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    if (H % P || T % P) return BA_ERR_SHAPE;
+    if ((key_padding_mask && kpm_ld < T) || (attn_mask && am_ld < T)) return BA_ERR_ARG;
+    if ((long long)B * H * T == 0) return BA_OK;
+    if (!q_tok || !k_tok || !v_tok || !out_tok || !lse_tok) return BA_ERR_ARG;
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    const bool masks = key_padding_mask || attn_mask;
+    Scratch ws;
+    const size_t need = ulysses_attn_fwd_workspace_size(P, H, B, T, d, dtype, masks);
+    if ((rc = ws.acquire(workspace, workspace_bytes, need, stream))) return rc;
+    uint8_t *wp = static_cast<uint8_t *>(ws.ptr);
+    const size_t eb = elem_size(dtype), tensor = (size_t)B * H * T * d * eb;
+    void *qh = wp, *kh = wp + align256(tensor), *vh = wp + 2 * align256(tensor), *oh = wp + 3 * align256(tensor);
+    float *lh = reinterpret_cast<float *>(wp + 4 * align256(tensor));
+    uint8_t *aws = wp + 4 * align256(tensor) + align256((size_t)B * H * T * 4);
+    const size_t aws_bytes = need - (size_t)(aws - wp);
+    // 1. first all-to-all: token-split -> head-split (P, H/P, B, T, d) for q, k, v
+    const void *srcs[3] = {q_tok, k_tok, v_tok};
+    void *dsts[3] = {qh, kh, vh};
+    for (int i = 0; i < 3; ++i)
+        if ((rc = ulysses_all_to_all(srcs[i], dsts[i], P, H, B, T, d, (int)eb, BA_A2A_TOKEN_TO_HEAD, stream)))
+            return rc;
+    // 2. attention over the full context of every head: the head-split array is a
+    //    (B, H, T, d) view with sB = T d, sH = B T d (one launch for all ranks)
+    const int64_t sB = (int64_t)T * d, sH = (int64_t)B * T * d, sT = d;
+    rc = ring_attn_fwd(ba_tensor{qh, sB, sH, sT}, ba_tensor{kh, sB, sH, sT}, ba_tensor{vh, sB, sH, sT}, B, H, T, d,
+                       dtype, 1, BA_PART_CONTIGUOUS, BA_MODE_FUSED, key_padding_mask, kpm_ld, attn_mask, am_ld,
+                       causal, scale, 0, 0.f, oh, dtype, lh, nullptr, aws, aws_bytes, stream);
+    if (rc) return rc;
+    // 3. reverse all-to-all of out (B, H, T, d) and lse (B, H, T) into token-split arrays
+    ba::UlyssesArgs u;
+    u.P = P;
+    u.H = H;
+    u.B = B;
+    u.Tl = T / P;
+    u.to_head = 0;
+    u.tok = out_tok;
+    u.head = oh;
+    u.elem_bytes = (int)eb;
+    u.row_bytes = (long long)d * eb;
+    u.sT = d;
+    u.sH = (long long)T * d;
+    u.sB = (long long)H * T * d;
+    if ((rc = ba::launch_ulysses_a2a(u, g_num_sms[dev], stream))) return rc;
+    u.tok = lse_tok;
+    u.head = lh;
+    u.elem_bytes = 4;
+    u.row_bytes = 4;
+    u.sT = 1;
+    u.sH = T;
+    u.sB = (long long)H * T;
+    return ba::launch_ulysses_a2a(u, g_num_sms[dev], stream);
+}
+
 // Same work as attn_block_fwd, with the tile-class map in the library's fixed
 // device array instead of a workspace: nothing is allocated.
 int attn_block_fwd_noalloc(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,

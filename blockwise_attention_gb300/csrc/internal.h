@@ -59,6 +59,20 @@ struct BwdArgs {
 
 int launch_attn_bwd(const BwdArgs &a, int num_sms, cudaStream_t s);
 
+// One Ulysses exchange: the token-split stacked array (P, H, B, Tl, d),
+// contiguous, against a strided (B, H, T = P Tl, d) view of the head side.
+struct UlyssesArgs {
+    void *tok;                // token-split array
+    void *head;               // head-side view base
+    long long sB, sH, sT;     // head-side element strides (d contiguous)
+    int P, H, B, Tl;
+    long long row_bytes;      // d * elem_bytes
+    int elem_bytes;
+    int to_head;              // 1: token-split -> head side, 0: head side -> token-split
+};
+
+int launch_ulysses_a2a(const UlyssesArgs &a, int num_sms, cudaStream_t s);
+
 // TMA descriptors of Q, K, V for the tensor-core kernel.
 struct TmaMaps {
     CUtensorMap q, k, v;

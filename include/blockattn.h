@@ -219,6 +219,48 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
                   void *workspace, size_t workspace_bytes, ba_stream_t stream);
 
 /*
+ * Ulysses ("Sequence/context parallelism" (brunomaga), section "Ulysses
+ * sequence parallelism"; "Change token partitions into head partitions with
+ * Ulysses"): P ranks first hold token shards, an all-to-all turns them into
+ * head shards holding the full context of H/P heads each, attention runs
+ * unchanged per head, and a reverse all-to-all returns the output to token
+ * shards.  On one GPU the ranks' buffers are stacked along a leading P axis.
+ *
+ * ulysses_all_to_all -- one exchange of whole d-rows (a permutation, exact):
+ *  BA_A2A_TOKEN_TO_HEAD: src (P, H, B, T/P, d) -> dst (P, H/P, B, T, d), where
+ *    rank r of dst holds heads [r H/P, (r+1) H/P) for tokens 0..T-1 in order;
+ *  BA_A2A_HEAD_TO_TOKEN: the inverse.
+ *  Both arrays contiguous, elem_bytes in {1, 2, 4, 8}, caller-owned, must not
+ *  overlap.  Errors: BA_ERR_SHAPE unless P divides H and T; BA_ERR_ARG for bad
+ *  sizes, direction or NULL pointers.
+ */
+#define BA_A2A_TOKEN_TO_HEAD 0
+#define BA_A2A_HEAD_TO_TOKEN 1
+int ulysses_all_to_all(const void *src, void *dst, int P, int H, int B, int T, int d,
+                       int elem_bytes, int direction, ba_stream_t stream);
+
+/*
+ * ulysses_attn_fwd -- Ulysses attention over P emulated ranks: the first
+ * all-to-all of q, k, v, one attention launch over every head's full context
+ * (the tensor-core kernel for bf16 d in {64, 128}), and the reverse all-to-all
+ * of out and lse.
+ *  q_tok, k_tok, v_tok: (P, H, B, T/P, d) contiguous token shards, dtype.
+ *  masks, causal, scale: as for ring_attn_fwd (global token positions).
+ *  out_tok: (P, H, B, T/P, d) contiguous, dtype; lse_tok: (P, H, B, T/P) fp32.
+ *  workspace: ulysses_attn_fwd_workspace_size() bytes (head-split q, k, v and
+ *    out, lse, and the attention's own scratch).
+ * Errors: BA_ERR_SHAPE unless P divides H and T and d is supported; BA_ERR_ARG
+ * as for ring_attn_fwd.
+ */
+size_t ulysses_attn_fwd_workspace_size(int P, int H, int B, int T, int d, int dtype, int has_masks);
+int ulysses_attn_fwd(const void *q_tok, const void *k_tok, const void *v_tok,
+                     int P, int H, int B, int T, int d, int dtype,
+                     const uint8_t *key_padding_mask, int64_t kpm_ld,
+                     const uint8_t *attn_mask, int64_t am_ld,
+                     int causal, float scale, void *out_tok, float *lse_tok,
+                     void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
  * rope_apply -- rotary position embedding ("RoFormer", item #4 of ai.engineer
  * "Transformers and Attention"): split each d-vector into coordinate pairs
  * (2c, 2c+1) and rotate pair c by the angle m * base^(-2c/d), m the token

@@ -587,7 +587,7 @@ def ulysses_arm(args, w, rank, world, local_rank):
                        "causal": w.causal, "visible_pairs": pairs, "flops_per_step": flops,
                        "l2": "inputs larger than the 129 MB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "a2a_kernel (token->head)",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "a2a_span_kernel (token->head)",
                          "algorithmic_bytes": a2a_bytes, "kernel_ms": a2a_ms,
                          "peak_source": f"{src} hbm_gbs (copy)"},
             "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": 7 * args.steps}

@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses"],
+    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses", "decode"],
                     help="ulysses: time ulysses_attn_fwd over P head-partitioned ranks (not the default line)")
     ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
                     help="backward: time ring_attn_bwd instead (not the default bench line)")
@@ -594,6 +594,68 @@ def ulysses_arm(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_arm(args, rank, world, local_rank):
+    """Time attn_decode_fwd on the decode workload (one query token per sequence,
+    B=8, H=32, d=128, bf16, 64K-slot cache with ragged lengths).  Bound by HBM:
+    `value` is the cache bytes read per second (every valid K and V byte once),
+    against the measured HBM copy peak."""
+    import blockwise_attention_gb300 as ba
+    from blockwise_attention_gb300.workloads import DECODE, make_decode_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    inp = make_decode_inputs(dev)
+    B, H, S, d = inp.k.shape
+    out = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    need = ba.load().attn_decode_workspace_size(B, H, S, d, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    total_len = int(inp.lengths.sum().item())
+    kv_bytes = 2.0 * total_len * H * d * 2
+    io_bytes = kv_bytes + 2.0 * B * H * d * 2 + B * H * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ba.attn_decode_fwd(inp.q, inp.k, inp.v, lengths=inp.lengths, out=out, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ba.sync_status() != 0:
+        raise RuntimeError("device status error after warm-up")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    gbs = io_bytes / (ms * 1e-3) / 1e9
+    line = {"metric": "decode attention: KV-cache bytes read per second (one query token per sequence)",
+            "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "decode_kv_64k", **{k: v for k, v in DECODE.items() if k != "seed"},
+                       "valid_keys_total": total_len, "bytes_per_step": io_bytes,
+                       "l2": "cache (8.6 GB) far larger than the 129 MB L2; no flush"},
+            "tokens_per_s": world * B / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "decode_split_kernel + decode_combine_kernel",
+                         "peak_source": f"{src} hbm_gbs (copy)"},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from blockwise_attention_gb300.workloads import WORKLOADS
@@ -611,6 +673,8 @@ def main():
             backward_arm(args, w, rank, world, local_rank)
         elif args.variant == "ulysses":
             ulysses_arm(args, w, rank, world, local_rank)
+        elif args.variant == "decode":
+            decode_arm(args, rank, world, local_rank)
         else:
             native_arm(args, w, rank, world, local_rank)
     finally:

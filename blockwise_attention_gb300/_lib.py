@@ -20,7 +20,7 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "libblockattn.so")
-_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu", "ulysses.cu"]
+_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu", "ulysses.cu", "decode.cu"]
 _HEADERS = ["common.cuh", "internal.h", "epilogue.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -97,7 +97,8 @@ EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ri
             "ring_attn_fwd_workspace_size", "rope_apply", "ba_tile_classes", "ba_index_maps",
             "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc",
             "attn_block_bwd", "attn_block_bwd_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
-            "ulysses_all_to_all", "ulysses_attn_fwd", "ulysses_attn_fwd_workspace_size"]
+            "ulysses_all_to_all", "ulysses_attn_fwd", "ulysses_attn_fwd_workspace_size",
+            "attn_decode_fwd", "attn_decode_workspace_size"]
 
 
 def load(path: str | None = None):
@@ -153,6 +154,10 @@ def load(path: str | None = None):
     lib.ulysses_attn_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.ulysses_attn_fwd.restype = i
     lib.ulysses_attn_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, i64, vp, i64, i, f, vp, vp, vp, sz, vp]
+    lib.attn_decode_workspace_size.restype = sz
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+    lib.attn_decode_fwd.restype = i
+    lib.attn_decode_fwd.argtypes = [T, T, T, i, i, i, i, i, vp, i, f, vp, i, vp, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -439,6 +444,36 @@ def ulysses_attn_fwd(q_tok, k_tok, v_tok, *, key_padding_mask=None, attn_mask=No
                               int(bool(causal)), 0.0 if scale is None else float(scale), _ptr(out), _ptr(lse),
                               _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream))
     _check("ulysses_attn_fwd", rc)
+    return out, lse
+
+
+def attn_decode_fwd(q, k_cache, v_cache, *, lengths=None, num_splits=0, scale=None, out=None, out_dtype=None,
+                    lse=None, workspace=None, stream=None):
+    """Decode attention of q (B, H, 1, d) against k_cache, v_cache (B, H, S, d),
+    split along the keys and merged by the LSE rule; lengths: int32 (B) CUDA
+    tensor of valid cache lengths or None.  Returns (out, lse)."""
+    lib = load()
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query per (b, h): q of shape (B, H, 1, d)")
+    S = k_cache.shape[2]
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else q.dtype
+    if out is None:
+        out = torch.empty((B, H, 1, d), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    _check_out(out, lse, (B, H, 1, d))
+    if lengths is not None and (lengths.dtype != torch.int32 or not lengths.is_cuda or lengths.numel() != B):
+        raise ValueError("lengths must be an int32 CUDA tensor of B entries")
+    need = lib.attn_decode_workspace_size(B, H, S, d, int(num_splits))
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib.attn_decode_fwd(_tensor(q), _tensor(k_cache), _tensor(v_cache), B, H, S, d, _dtype_code(q.dtype),
+                             _ptr(lengths), int(num_splits), 0.0 if scale is None else float(scale), _ptr(out),
+                             _dtype_code(out.dtype), _ptr(lse), _ptr(workspace),
+                             0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("attn_decode_fwd", rc)
     return out, lse
 
 

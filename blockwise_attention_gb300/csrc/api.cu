@@ -1092,6 +1092,91 @@ int ulysses_attn_fwd(const void *q_tok, const void *k_tok, const void *v_tok, in
     return ba::launch_ulysses_a2a(u, g_num_sms[dev], stream);
 }
 
+// ---------------------------------------------------------------------------
+// Decode with a split KV cache
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int decode_splits(int B, int H, int S, int num_splits, int num_sms) {
+    if (num_splits > 0) return num_splits < S ? num_splits : (S > 0 ? S : 1);
+    const long long bh = (long long)B * H > 0 ? (long long)B * H : 1;
+    long long n = (4LL * num_sms + bh - 1) / bh;   // about four CTAs per SM
+    const long long cap = (S + 63) / 64 > 0 ? (S + 63) / 64 : 1;   // at least 64 keys per split
+    if (n > cap) n = cap;
+    if (n < 1) n = 1;
+    return (int)n;
+}
+
+bool rows16(const void *p, long long sB, long long sH, long long sT, size_t eb) {
+    return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && (sB * (long long)eb) % 16 == 0 &&
+           (sH * (long long)eb) % 16 == 0 && (sT * (long long)eb) % 16 == 0;
+}
+
+}  // namespace
+
+size_t attn_decode_workspace_size(int B, int H, int S, int d, int num_splits) {
+    if (B < 0 || H < 0 || S < 0 || d < 1) return 0;
+    const int n = decode_splits(B, H, S, num_splits, 152);
+    const int dev = current_device();
+    const int n_dev = dev >= 0 && g_num_sms[dev] > 0 ? decode_splits(B, H, S, num_splits, g_num_sms[dev]) : n;
+    const int nn = n > n_dev ? n : n_dev;
+    return align256((size_t)B * H * nn * d * 4) + align256((size_t)B * H * nn * 4);
+}
+
+int attn_decode_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int S, int d, int dtype,
+                    const int32_t *lengths, int num_splits, float scale, void *out, int out_dtype, float *lse,
+                    void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+    if (B < 0 || H < 0 || S < 0 || num_splits < 0 || !valid_dtype(dtype)) return BA_ERR_ARG;
+    if (!valid_d(d)) return BA_ERR_SHAPE;
+    if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
+    if ((long long)B * H == 0) return BA_OK;
+    if (check_tensor(q) || !out || !lse || (S > 0 && (check_tensor(k) || check_tensor(v)))) return BA_ERR_ARG;
+    const size_t eb = elem_size(dtype);
+    q = fix_unit_strides(q, B, H, 1, d);
+    k = fix_unit_strides(k, B, H, S, d);
+    v = fix_unit_strides(v, B, H, S, d);
+    if (!rows16(q.ptr, q.sB, q.sH, d, eb) || (S > 0 && (!rows16(k.ptr, k.sB, k.sH, k.sT, eb) ||
+                                                         !rows16(v.ptr, v.sB, v.sH, v.sT, eb))))
+        return BA_ERR_ARG;   // the kernel reads 16-byte vectors of every row
+    const int dev = current_device();
+    if (dev < 0) return BA_ERR_CUDA;
+    int rc = device_setup(dev);
+    if (rc) return rc;
+    ba::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.B = B;
+    a.H = H;
+    a.S = S;
+    a.d = d;
+    a.dtype = dtype;
+    a.q = q.ptr;
+    a.qsB = q.sB;
+    a.qsH = q.sH;
+    a.k = k.ptr;
+    a.ksB = k.sB;
+    a.ksH = k.sH;
+    a.ksT = k.sT;
+    a.v = v.ptr;
+    a.vsB = v.sB;
+    a.vsH = v.sH;
+    a.vsT = v.sT;
+    a.lengths = lengths;
+    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
+    a.n_splits = decode_splits(B, H, S, num_splits, g_num_sms[dev]);
+    a.split_len = S > 0 ? (S + a.n_splits - 1) / a.n_splits : 1;
+    Scratch ws;
+    const size_t need = align256((size_t)B * H * a.n_splits * d * 4) + align256((size_t)B * H * a.n_splits * 4);
+    if ((rc = ws.acquire(workspace, workspace_bytes, need, stream))) return rc;
+    a.part_o = static_cast<float *>(ws.ptr);
+    a.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(ws.ptr) +
+                                           align256((size_t)B * H * a.n_splits * d * 4));
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse;
+    return ba::launch_decode(a, stream);
+}
+
 // Same work as attn_block_fwd, with the tile-class map in the library's fixed
 // device array instead of a workspace: nothing is allocated.
 int attn_block_fwd_noalloc(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int Lq, int Lk, int d, int dtype,

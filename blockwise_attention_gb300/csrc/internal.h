@@ -73,6 +73,23 @@ struct UlyssesArgs {
 
 int launch_ulysses_a2a(const UlyssesArgs &a, int num_sms, cudaStream_t s);
 
+// Decode attention of one query per (b, h) against a KV cache, in key splits.
+struct DecodeArgs {
+    int B, H, S, d, dtype;
+    const void *q, *k, *v;               // q: (B, H, 1, d); k, v: (B, H, S, d), element strides
+    long long qsB, qsH;
+    long long ksB, ksH, ksT, vsB, vsH, vsT;
+    const int32_t *lengths;              // (B) valid cache lengths, or nullptr = S
+    float scale;
+    int split_len, n_splits;
+    float *part_o, *part_lse;            // (B*H, n_splits, d), (B*H, n_splits) fp32 partials
+    void *out;                           // (B, H, 1, d) contiguous, out_dtype
+    int out_dtype;
+    float *lse;                          // (B, H, 1)
+};
+
+int launch_decode(const DecodeArgs &a, cudaStream_t s);
+
 // TMA descriptors of Q, K, V for the tensor-core kernel.
 struct TmaMaps {
     CUtensorMap q, k, v;

@@ -115,3 +115,31 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs
     if w.band is not None:
         am = band_cls_mask(w.T, w.band, device=device)
     return Inputs(q, k, v, lengths, kpm, am)
+
+
+@dataclass
+class DecodeInputs:
+    q: torch.Tensor          # (B, H, 1, d)
+    k: torch.Tensor          # (B, H, S, d) cache
+    v: torch.Tensor
+    lengths: torch.Tensor    # int32 (B), valid cache lengths
+
+
+# Decode workload (one query token per sequence against a long KV cache):
+# B=8 sequences, H=32 heads, d=128, bf16, a 65536-slot cache per (b, h) whose
+# valid length is drawn uniformly in [32768, 65536] per sequence.
+DECODE = dict(B=8, H=32, S=65536, d=128, len_lo=32768, len_hi=65536, std=0.5, seed=2100)
+
+
+def make_decode_inputs(device="cpu", seed: Optional[int] = None, **over) -> DecodeInputs:
+    """Draw the seeded decode inputs (q, then the K cache, the V cache, then lengths)."""
+    cfg = dict(DECODE, **over)
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] if seed is None else seed)
+    B, H, S, d = cfg["B"], cfg["H"], cfg["S"], cfg["d"]
+    q = (torch.randn((B, H, 1, d), generator=g, device=device) * cfg["std"]).to(torch.bfloat16)
+    k = (torch.randn((B, H, S, d), generator=g, device=device) * cfg["std"]).to(torch.bfloat16)
+    v = torch.randn((B, H, S, d), generator=g, device=device).to(torch.bfloat16)
+    lengths = torch.randint(cfg["len_lo"], cfg["len_hi"] + 1, (B,), generator=g, device=device).to(torch.int32)
+    return DecodeInputs(q, k, v, lengths)

@@ -261,6 +261,30 @@ int ulysses_attn_fwd(const void *q_tok, const void *k_tok, const void *v_tok,
                      void *workspace, size_t workspace_bytes, ba_stream_t stream);
 
 /*
+ * attn_decode_fwd -- decode attention: one query token per (b, h) against a KV
+ * cache, split along the keys.  Decode processes one token at a time and
+ * shards the KV cache rather than the input tokens ("Sequence/context
+ * parallelism" (brunomaga), the note on the inference decode step); each split
+ * gives a partial (O, LSE) over its keys and the partials are merged by the LSE
+ * rule of attn_merge (an associative merge; here all splits at once).
+ *  q: (B, H, 1, d); k_cache, v_cache: (B, H, S, d) with element strides, every
+ *    row starting on a 16-byte boundary (BA_ERR_ARG otherwise).
+ *  lengths: NULL, or device int32[B]: keys [0, lengths[b]) of sequence b are
+ *    valid (clamped to [0, S]); a sequence of length 0 gets out = 0, lse = -inf.
+ *  num_splits: 0 = chosen by the library (about four CTAs per SM, at least 64
+ *    keys per split), else the number of key splits.
+ *  out: (B, H, 1, d) contiguous, out_dtype BA_F32 or dtype; lse: (B, H, 1) fp32.
+ *  workspace: attn_decode_workspace_size() bytes (fp32 partials).
+ * Bound by HBM: every valid K and V byte is read once.
+ */
+size_t attn_decode_workspace_size(int B, int H, int S, int d, int num_splits);
+int attn_decode_fwd(ba_tensor q, ba_tensor k_cache, ba_tensor v_cache,
+                    int B, int H, int S, int d, int dtype,
+                    const int32_t *lengths, int num_splits, float scale,
+                    void *out, int out_dtype, float *lse,
+                    void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
  * rope_apply -- rotary position embedding ("RoFormer", item #4 of ai.engineer
  * "Transformers and Attention"): split each d-vector into coordinate pairs
  * (2c, 2c+1) and rotate pair c by the angle m * base^(-2c/d), m the token

@@ -76,7 +76,7 @@ def _load():
                                              vp, i64, vp, i64, ctypes.c_int, f64, vp, vp, vp, vp, vp,
                                              ctypes.c_int]
         lib.oracle_rope.restype = ctypes.c_int
-        lib.oracle_rope.argtypes = [vp, i64, i64, i64, vp, f64, ctypes.c_int, vp, vp]
+        lib.oracle_rope.argtypes = [vp, i64, i64, i64, vp, f64, f64, ctypes.c_int, vp, vp]
         lib.oracle_round_bf16.restype = ctypes.c_float
         lib.oracle_round_bf16.argtypes = [f64]
         _lib = lib
@@ -211,9 +211,10 @@ def ulysses_head_to_token(x_head: np.ndarray, P: int) -> np.ndarray:
     return out
 
 
-def rope(x, base=10000.0, positions=None, round_to="bf16"):
+def rope(x, base=10000.0, positions=None, round_to="bf16", pos_scale=1.0):
     """Rotate coordinate pairs of x (..., T, d).  round_to: "bf16", "f32" or None
-    (None returns the unrounded float64 rotation)."""
+    (None returns the unrounded float64 rotation).  pos_scale multiplies the
+    position index before the angle is formed (Position Interpolation)."""
     lib = _load()
     xa = _f32(x)
     shape = xa.shape
@@ -222,10 +223,10 @@ def rope(x, base=10000.0, positions=None, round_to="bf16"):
     pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int64)
     if round_to is None:
         y = np.zeros(shape, dtype=np.float64)
-        rc = lib.oracle_rope(_ptr(xa), BH, T, d, _ptr(pos), float(base), 0, _ptr(y), None)
+        rc = lib.oracle_rope(_ptr(xa), BH, T, d, _ptr(pos), float(base), float(pos_scale), 0, _ptr(y), None)
     else:
         y = np.zeros(shape, dtype=np.float32)
-        rc = lib.oracle_rope(_ptr(xa), BH, T, d, _ptr(pos), float(base),
+        rc = lib.oracle_rope(_ptr(xa), BH, T, d, _ptr(pos), float(base), float(pos_scale),
                              2 if round_to == "bf16" else 1, None, _ptr(y))
     if rc != 0:
         raise ValueError("oracle_rope: bad arguments")
@@ -277,6 +278,10 @@ def partition(T: int, P: int, kind: str) -> np.ndarray:
     contiguous: rank r holds the r-th of P equal time blocks.
     zigzag: the sequence is cut into 2P equal chunks; rank r holds chunk r
     followed by chunk 2P-1-r (early and late tokens paired).
+    striped: token t belongs to rank t mod P, in order (rank r holds r, r+P,
+    r+2P, ...): the pages name Striped Attention as a permutation that
+    balances causal work; round-robin stripes of one token are the reading
+    taken here.
     """
     tok = np.zeros((P, T // P), dtype=np.int32)
     if kind == "contiguous":
@@ -292,6 +297,11 @@ def partition(T: int, P: int, kind: str) -> np.ndarray:
             for t in range(c):
                 tok[r, t] = r * c + t
                 tok[r, c + t] = (2 * P - 1 - r) * c + t
+    elif kind == "striped":
+        assert T % P == 0
+        for r in range(P):
+            for t in range(T // P):
+                tok[r, t] = t * P + r
     else:
         raise ValueError(kind)
     return tok

@@ -184,12 +184,15 @@ float oracle_round_bf16(double x) { return round_bf16(x); }
  * y32 != NULL.
  */
 int oracle_rope(const float *x, int64_t BH, int64_t T, int64_t d,
-                const int64_t *positions, double base, int round_mode,
+                const int64_t *positions, double base, double pos_scale, int round_mode,
                 double *y64, float *y32) {
     if (!x || d <= 0 || (d & 1)) return -1;
     for (int64_t r = 0; r < BH; ++r) {
         for (int64_t t = 0; t < T; ++t) {
-            double m = positions ? (double)positions[t] : (double)t;
+            /* Position Interpolation ("Extending Context Window of Large Language
+             * Models via Position Interpolation" summary, #59): the position index is
+             * rescaled before the rotary angle is formed; pos_scale = 1 is plain RoPE. */
+            double m = (positions ? (double)positions[t] : (double)t) * pos_scale;
             const float *xr = x + (r * T + t) * d;
             for (int64_t c = 0; c < d / 2; ++c) {
                 double theta = pow(base, -(double)(2 * c) / (double)d);

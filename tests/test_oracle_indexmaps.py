@@ -109,3 +109,18 @@ def test_tile_classes_match_vectorised_recount():
                     blk = vis[qt * tile:(qt + 1) * tile, kt * tile:(kt + 1) * tile]
                     want = oracle.EMPTY if not blk.any() else (oracle.FULL if blk.all() else oracle.PARTIAL)
                     assert cls[b, qt, kt] == want
+
+
+def test_striped_partition_brute_force_counts():
+    """Striped (round-robin) partition of T=8 over P=2: rank 0 holds the even
+    tokens, rank 1 the odd ones; causal pair counts by brute force are 16 / 20,
+    between contiguous (10 / 26) and zigzag (18 / 18)."""
+    tok = oracle.partition(8, 2, "striped")
+    assert tok.tolist() == [[0, 2, 4, 6], [1, 3, 5, 7]]
+    pairs = [sum(oracle.is_visible(0, int(i), j, True, None, None) for i in r for j in range(8)) for r in tok]
+    assert pairs == [16, 20]
+    # at 8K over 8 ranks the spread is one row's worth per rank step: max/min < 1.002
+    tok = oracle.partition(8192, 8, "striped")
+    p = [causal_pairs(r) for r in tok]
+    assert sorted(np.concatenate(tok).tolist()) == list(range(8192))
+    assert max(p) / min(p) < 1.002

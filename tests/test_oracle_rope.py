@@ -128,3 +128,35 @@ def test_rounded_output_is_rounding_of_fp64_result():
 def test_odd_dimension_rejected():
     with pytest.raises(ValueError):
         oracle.rope(np.zeros((2, 3), np.float32))
+
+
+def test_position_interpolation_rescales_the_index():
+    """Position Interpolation ("Extending Context Window of Large Language Models
+    via Position Interpolation" summary): positions are rescaled into the
+    original range before rotating.  Scale 1/4 at positions 4m is plain RoPE at
+    positions m, bit for bit (4m * 1/4 = m exactly); scale 1 is plain RoPE."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 50, 16)).astype(np.float32)
+    m = np.arange(50, dtype=np.int64) * 3 + 1
+    plain = oracle.rope(x, base=10000.0, positions=m, round_to=None)
+    pi = oracle.rope(x, base=10000.0, positions=4 * m, round_to=None, pos_scale=0.25)
+    assert np.array_equal(plain, pi)
+    assert np.array_equal(oracle.rope(x, positions=m, round_to=None, pos_scale=1.0), plain)
+    assert not np.array_equal(oracle.rope(x, positions=m, round_to=None, pos_scale=0.5), plain)
+
+
+def test_position_interpolation_keeps_relative_positions():
+    """With scale s, the dot product of a rotated query at m and key at n depends
+    only on (m - n) s: shifting both positions leaves it unchanged."""
+    rng = np.random.default_rng(22)
+    d = 8
+    q = rng.standard_normal((1, 1, d)).astype(np.float32)
+    k = rng.standard_normal((1, 1, d)).astype(np.float32)
+    s = 0.375
+    def dot(mq, nk):
+        a = oracle.rope(q, positions=np.array([mq]), round_to=None, pos_scale=s)
+        b = oracle.rope(k, positions=np.array([nk]), round_to=None, pos_scale=s)
+        return float(np.sum(a * b))
+    base_dot = dot(40, 11)
+    for shift in (1, 17, 1000):
+        assert abs(dot(40 + shift, 11 + shift) - base_dot) <= 1e-12

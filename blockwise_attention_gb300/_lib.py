@@ -29,7 +29,7 @@ BA_OK, BA_ERR_ARG, BA_ERR_SHAPE, BA_ERR_CUDA, BA_ERR_TIMEOUT, BA_ERR_UNSUPPORTED
 BA_ERR_NOALLOC_LIMIT = -7
 BA_NOALLOC_MAX_CLASS_BYTES = 1 << 20
 BA_F32, BA_BF16 = 0, 1
-PARTITIONS = {"contiguous": 0, "zigzag": 1}
+PARTITIONS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 MODES = {"stepwise": 0, "fused": 1}
 BA_TILE_EMPTY, BA_TILE_FULL, BA_TILE_PARTIAL = 0, 1, 2
 
@@ -129,7 +129,7 @@ def load(path: str | None = None):
     lib.ring_attn_fwd.argtypes = [T, T, T, i, i, i, i, i, i, i, i, vp, i64, vp, i64, i, f, i, f, vp, i, vp, vp,
                                   vp, sz, vp]
     lib.rope_apply.restype = i
-    lib.rope_apply.argtypes = [T, T, i, i, i, i, i, vp, f, vp, vp, vp]
+    lib.rope_apply.argtypes = [T, T, i, i, i, i, i, vp, f, f, vp, vp, vp]
     lib.ba_tile_classes.restype = i
     lib.ba_tile_classes.argtypes = [i, i, i, i64, i64, vp, i64, vp, i64, i, vp, vp]
     lib.ba_index_maps.restype = i
@@ -477,9 +477,10 @@ def attn_decode_fwd(q, k_cache, v_cache, *, lengths=None, num_splits=0, scale=No
     return out, lse
 
 
-def rope_apply(x, *, x2=None, base=10000.0, positions=None, out=None, out2=None, stream=None):
+def rope_apply(x, *, x2=None, base=10000.0, positions=None, pos_scale=1.0, out=None, out2=None, stream=None):
     """Rotary position embedding of x (B, H, T, d) into a contiguous output; with
-    x2 given, rotates x2 by the same launch and returns (y, y2)."""
+    x2 given, rotates x2 by the same launch and returns (y, y2).  pos_scale is
+    the Position Interpolation factor applied to the position index."""
     lib = load()
     B, H, T, d = x.shape
     if out is None:
@@ -493,7 +494,7 @@ def rope_apply(x, *, x2=None, base=10000.0, positions=None, out=None, out2=None,
         raise ValueError("positions: int32 CUDA tensor")
     t2 = _tensor(x2) if x2 is not None else ba_tensor(None, 0, 0, 0)
     _check("rope_apply", lib.rope_apply(_tensor(x), t2, B, H, T, d, _dtype_code(x.dtype), _ptr(positions),
-                                        float(base), _ptr(out), _ptr(out2), _stream(stream)))
+                                        float(base), float(pos_scale), _ptr(out), _ptr(out2), _stream(stream)))
     return out if x2 is None else (out, out2)
 
 

@@ -218,6 +218,7 @@ struct RopeArgs {
     int n;
     int B, H, T, d;
     const int32_t *positions;
+    double pos_scale;       // Position Interpolation: angle = (position * pos_scale) * theta
     Thetas th;
 };
 
@@ -293,7 +294,7 @@ __global__ void rope_bf16_kernel(const RopeArgs a) {
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e / groups), c0 = (int)(e % groups) * 4;
-        const double m = a.positions ? (double)a.positions[t] : (double)t;
+        const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
         Split4 cs[4], sn[4], ncs[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -350,7 +351,7 @@ __global__ void rope_f32_kernel(const RopeArgs a) {
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e / half), c = (int)(e % half);
-        const double m = a.positions ? (double)a.positions[t] : (double)t;
+        const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
         double sn, cs;
         sincos(m * a.th.th[c], &sn, &cs);
         for (int ti = 0; ti < a.n; ++ti) {
@@ -378,7 +379,7 @@ __global__ void rope_bf16_pair_kernel(const RopeArgs a) {
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(e / half), c = (int)(e % half);
-        const double m = a.positions ? (double)a.positions[t] : (double)t;
+        const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
         double sn, cs;
         sincos(m * a.th.th[c], &sn, &cs);
         for (int ti = 0; ti < a.n; ++ti) {
@@ -453,7 +454,7 @@ int run_tile_classes(const Geom &g, int8_t *cls, cudaStream_t s) {
 
 // Rotate one or two (B, H, T, d) tensors (x2 / y2 may be null) into contiguous outputs.
 int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, int d, int dtype,
-                const int32_t *pos, float base, void *y, void *y2, cudaStream_t s) {
+                const int32_t *pos, float base, float pos_scale, void *y, void *y2, cudaStream_t s) {
     RopeArgs a;
     std::memset(&a, 0, sizeof a);
     for (int c = 0; c < d / 2; ++c) a.th.th[c] = std::pow((double)base, -(double)(2 * c) / (double)d);
@@ -475,6 +476,7 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
     a.T = T;
     a.d = d;
     a.positions = pos;
+    a.pos_scale = pos_scale > 0.f ? (double)pos_scale : 1.0;   // a float times an int32 is exact in fp64
     if ((long long)T * d == 0 || B == 0 || H == 0) return BA_OK;
     const int threads = 256;
     const long long per = dtype == BA_BF16 && d % 8 == 0 ? d / 8 : d / 2;
@@ -530,7 +532,8 @@ const char *ba_strerror(int code) {
 
 int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule) {
     if (T < 0 || P < 1) return BA_ERR_ARG;
-    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG && partition != BA_PART_STRIPED)
+        return BA_ERR_ARG;
     const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
     if (T % NC) return BA_ERR_SHAPE;
     const int CL = T / NC, per = T / P;
@@ -542,6 +545,8 @@ int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedul
                 int tok;
                 if (partition == BA_PART_CONTIGUOUS)
                     tok = r * CL + t;
+                else if (partition == BA_PART_STRIPED)
+                    tok = t * P + r;
                 else
                     tok = t < CL ? c0 * CL + t : c1 * CL + (t - CL);
                 tok_of[(long long)r * per + t] = tok;
@@ -599,16 +604,18 @@ int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_
 }
 
 int rope_apply(ba_tensor x, ba_tensor x2, int B, int H, int T, int d, int dtype, const int32_t *positions,
-               float base, void *y, void *y2, ba_stream_t stream) {
+               float base, float pos_scale, void *y, void *y2, ba_stream_t stream) {
     if (B < 0 || H < 0 || T < 0 || d < 2 || (d & 1) || d > 128 || !valid_dtype(dtype) || !(base > 0.f))
         return BA_ERR_ARG;
+    if (pos_scale < 0.f || !(pos_scale == pos_scale)) return BA_ERR_ARG;
     const bool two = x2.ptr != nullptr || y2 != nullptr;
     if ((long long)B * H * T > 0 && (!x.ptr || !y || (two && (!x2.ptr || !y2)))) return BA_ERR_ARG;
     const int dev = current_device();
     if (dev < 0) return BA_ERR_CUDA;
     int rc = device_setup(dev);
     if (rc) return rc;
-    return launch_rope(x, two ? &x2 : nullptr, B, H, T, d, dtype, positions, base, y, two ? y2 : nullptr, stream);
+    return launch_rope(x, two ? &x2 : nullptr, B, H, T, d, dtype, positions, base, pos_scale, y,
+                       two ? y2 : nullptr, stream);
 }
 
 int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off, const uint8_t *key_padding_mask,
@@ -741,6 +748,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     if (B < 0 || H < 0 || T < 0 || P < 1 || !valid_dtype(dtype)) return BA_ERR_ARG;
     if ((long long)B * H * T > 0 && (check_tensor(q) || check_tensor(k) || check_tensor(v) || !out || !lse))
         return BA_ERR_ARG;
+    if (partition == BA_PART_STRIPED) return BA_ERR_UNSUPPORTED;   // tokens of a rank are not a position range
     if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
     if (mode != BA_MODE_STEPWISE && mode != BA_MODE_FUSED) return BA_ERR_ARG;
     if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
@@ -810,7 +818,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
         wp += align256(tensor * elem_size(dtype));
         void *kr = wp;
         wp += align256(tensor * elem_size(dtype));
-        if ((rc = launch_rope(q, &k, B, H, T, d, dtype, nullptr, rope_base, qr, kr, stream))) return rc;
+        if ((rc = launch_rope(q, &k, B, H, T, d, dtype, nullptr, rope_base, 1.f, qr, kr, stream))) return rc;
         const long long sT = d, sH = (long long)T * d, sB = (long long)H * T * d;
         q = ba_tensor{qr, sB, sH, sT};
         k = ba_tensor{kr, sB, sH, sT};
@@ -933,6 +941,7 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
     int rc = check_bwd_common(q, k, v, out, dout, lse, B, H, T, T, d, dtype, dq, dk, dv);
     if (rc) return rc;
     if (P < 1) return BA_ERR_ARG;
+    if (partition == BA_PART_STRIPED) return BA_ERR_UNSUPPORTED;   // tokens of a rank are not a position range
     if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
     if (mode != BA_MODE_STEPWISE && mode != BA_MODE_FUSED) return BA_ERR_ARG;
     if ((key_padding_mask && kpm_ld < T) || (attn_mask && am_ld < T)) return BA_ERR_ARG;

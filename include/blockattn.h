@@ -64,7 +64,11 @@ enum {
 };
 
 enum { BA_F32 = 0, BA_BF16 = 1 };
-enum { BA_PART_CONTIGUOUS = 0, BA_PART_ZIGZAG = 1 };
+/* Token partitions over P ranks: contiguous blocks, zigzag (2P chunks, rank r
+ * holds chunks r and 2P-1-r), and striped (token t on rank t mod P; index maps
+ * only: ring_attn_fwd / ring_attn_bwd return BA_ERR_UNSUPPORTED for it, since a
+ * rank's tokens are not a range of positions). */
+enum { BA_PART_CONTIGUOUS = 0, BA_PART_ZIGZAG = 1, BA_PART_STRIPED = 2 };
 enum { BA_MODE_STEPWISE = 0, BA_MODE_FUSED = 1 };
 enum { BA_TILE_EMPTY = 0, BA_TILE_FULL = 1, BA_TILE_PARTIAL = 2 };
 
@@ -297,9 +301,15 @@ int attn_decode_fwd(ba_tensor q, ba_tensor k_cache, ba_tensor v_cache,
  *  same shape rotated by the same launch (e.g. K next to Q); pass
  *  x2.ptr = NULL and y2 = NULL for one tensor.  positions: NULL (position of
  *  row t is t) or device int32[T].  d must be even and <= 128 (else BA_ERR_ARG).
+ *  pos_scale: Position Interpolation ("Extending Context Window of Large
+ *  Language Models via Position Interpolation", item #59): the position index
+ *  is multiplied by pos_scale (e.g. original / extended window) before the
+ *  angle is formed, m' = m * pos_scale in fp64 (exact); 0 or 1 = plain RoPE,
+ *  negative or NaN = BA_ERR_ARG.
  */
 int rope_apply(ba_tensor x, ba_tensor x2, int B, int H, int T, int d, int dtype,
-               const int32_t *positions, float base, void *y, void *y2, ba_stream_t stream);
+               const int32_t *positions, float base, float pos_scale, void *y, void *y2,
+               ba_stream_t stream);
 
 /*
  * ba_tile_classes -- class of each 128 x 128 tile of the combined exclusion

@@ -38,6 +38,7 @@ def test_strerror():
 
 
 @pytest.mark.parametrize("T,P,kind", [(8, 4, "contiguous"), (8, 2, "zigzag"), (8, 2, "contiguous"),
+                                      (8, 2, "striped"), (8192, 8, "striped"), (12, 3, "striped"),
                                       (1024, 4, "contiguous"), (8192, 8, "zigzag"), (65536, 16, "zigzag"),
                                       (512, 2, "contiguous"), (1000, 4, "zigzag"), (96, 3, "zigzag"),
                                       (7, 1, "contiguous")])
@@ -73,7 +74,12 @@ def test_argument_errors_are_host_side():
     assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 12, 64, 1, 4, 1, 1, None, 0, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
                              dummy, None, None, 0, None) == _lib.BA_ERR_SHAPE
     # ring: odd d with rope
-    assert lib.rope_apply(T1, T0, 1, 1, 8, 7, 1, None, 1e4, dummy, None, None) == _lib.BA_ERR_ARG
+    assert lib.rope_apply(T1, T0, 1, 1, 8, 7, 1, None, 1e4, 1.0, dummy, None, None) == _lib.BA_ERR_ARG
+    # negative Position Interpolation scale
+    assert lib.rope_apply(T1, T0, 1, 1, 8, 8, 1, None, 1e4, -0.5, dummy, None, None) == _lib.BA_ERR_ARG
+    # striped partitions have index maps but no ring kernel
+    assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 16, 64, 1, 4, 2, 1, None, 0, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
+                             dummy, None, None, 0, None) == _lib.BA_ERR_UNSUPPORTED
     assert lib.attn_merge(None, dummy, dummy, dummy, 4, 4, None) == _lib.BA_ERR_ARG
     # backward: NULL out, unsupported d, T not divisible by 2P, masks not covering positions
     assert lib.attn_block_bwd(T1, T1, T1, T0, T1, dummy, 1, 1, 8, 8, 64, 1, 0, 0, None, 0, None, 0, 0, 0.0,

@@ -207,3 +207,19 @@ def test_workspace_reuse_and_alignment(mode):
     out, lse = ba.attn_block_fwd(q, k, v, causal=True, workspace=ws, out_dtype=torch.float32)
     o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=True)
     compare(out, lse, o_ref, l_ref, "bf16", "block with caller workspace")
+
+
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("bf16", 6), ("f32", 64)])
+@pytest.mark.parametrize("scale", [0.25, float(np.float32(0.3)), 0.125])
+def test_rope_position_interpolation_bit_exact(dt, d, scale):
+    """Position Interpolation: the position index times pos_scale before the angle;
+    bit-exact against the fp64 oracle rounded once (the scale as the ABI's fp32)."""
+    B, H, T = 2, 3, 500
+    x = rand((B, H, T, d), DT[dt], 60)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda") * 8 + 3
+    y = ba.rope_apply(x, base=10000.0, positions=pos, pos_scale=scale)
+    ref = oracle.rope(x.float().cpu(), base=10000.0, positions=pos.cpu().numpy(), round_to=dt, pos_scale=scale)
+    assert np.array_equal(y.float().cpu().numpy(), ref)
+    # scale 1/4 at positions 4m reproduces plain RoPE at m
+    m = torch.arange(T, dtype=torch.int32, device="cuda")
+    assert torch.equal(ba.rope_apply(x, positions=4 * m, pos_scale=0.25), ba.rope_apply(x, positions=m))

@@ -3,7 +3,7 @@
 // Decode processes one query token per sequence and shards the KV cache rather
 // than the input tokens ("Sequence/context parallelism" (brunomaga), the note
 // on the inference decode step); a sequence's cache grows as tokens arrive
-// (ai.engineer "Transformers and Attention", KV caches).  The cache of one
+// ("Transformers and Attention" (ai.engineer), item #57 on KV-cache allocation).  The cache of one
 // (b, h) is cut into key splits; each split yields a partial attention (O, LSE)
 // over its keys, and the partials are merged by the LSE rule, never added or
 // averaged (brunomaga, "Circulate K/V blocks with Ring": the merge of

@@ -77,7 +77,8 @@ def visible_pairs(w, inp) -> int:
     return total * w.H
 
 
-KERNEL_SOURCES = ["blockwise_attention_gb300/csrc/attn_tc.cu", "blockwise_attention_gb300/csrc/common.cuh",
+KERNEL_SOURCES = ["blockwise_attention_gb300/csrc/attn_tc.cu", "blockwise_attention_gb300/csrc/tc_ptx.cuh",
+                  "blockwise_attention_gb300/csrc/common.cuh",
                   "blockwise_attention_gb300/csrc/epilogue.cuh", "blockwise_attention_gb300/csrc/internal.h"]
 
 

@@ -20,8 +20,8 @@ _ROOT = os.path.dirname(_PKG)
 _CSRC = os.path.join(_PKG, "csrc")
 _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "libblockattn.so")
-_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu", "ulysses.cu", "decode.cu"]
-_HEADERS = ["common.cuh", "internal.h", "epilogue.cuh"]
+_SOURCES = ["api.cu", "attn_simt.cu", "attn_tc.cu", "attn_bwd.cu", "attn_bwd_tc.cu", "ulysses.cu", "decode.cu"]
+_HEADERS = ["common.cuh", "internal.h", "epilogue.cuh", "tc_ptx.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 BA_OK, BA_ERR_ARG, BA_ERR_SHAPE, BA_ERR_CUDA, BA_ERR_TIMEOUT, BA_ERR_UNSUPPORTED, BA_ERR_WORKSPACE = \

@@ -868,6 +868,28 @@ namespace {
 
 ba::TensorRef tref(const ba_tensor &t) { return ba::TensorRef{t.ptr, t.sB, t.sH, t.sT}; }
 
+// The tensor-core backward for bf16 with d in {64, 128} when every operand can
+// be read by TMA; the CUDA-core kernels otherwise.
+int run_bwd(ba::BwdArgs &a, ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor dout, long long q_rows,
+            long long k_rows, int dev, cudaStream_t s) {
+    a.err = g_err_ptr[dev];
+    a.wait_limit_ns = kWaitLimitNs;
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };   // float4 epilogues
+    if (ba::bwd_tc_supported(a.dtype, a.d) && q_rows > 0 && k_rows > 0 && tma_ok(q, a.B, a.H) &&
+        tma_ok(k, a.B, a.H) && tma_ok(v, a.B, a.H) && tma_ok(dout, a.B, a.H) && al16(a.dq) && al16(a.dk) &&
+        al16(a.dv)) {
+        int rc = get_encoder();
+        if (rc) return rc;
+        ba::BwdMaps m;
+        if ((rc = encode_map(&m.q, q.ptr, a.d, q_rows, a.H, a.B, q.sT, q.sH, q.sB))) return rc;
+        if ((rc = encode_map(&m.dout, dout.ptr, a.d, q_rows, a.H, a.B, dout.sT, dout.sH, dout.sB))) return rc;
+        if ((rc = encode_map(&m.k, k.ptr, a.d, k_rows, a.H, a.B, k.sT, k.sH, k.sB))) return rc;
+        if ((rc = encode_map(&m.v, v.ptr, a.d, k_rows, a.H, a.B, v.sT, v.sH, v.sB))) return rc;
+        return ba::launch_attn_bwd_tc(a, m, g_num_sms[dev], s);
+    }
+    return ba::launch_attn_bwd(a, g_num_sms[dev], s);
+}
+
 int check_bwd_common(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout, const float *lse,
                      int B, int H, int Lq, int Lk, int d, int dtype, const float *dq, const float *dk,
                      const float *dv) {
@@ -917,11 +939,16 @@ int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tens
     a.kpm_ld = kpm_ld;
     a.am = attn_mask;
     a.am_ld = am_ld;
-    a.q = tref(fix_unit_strides(q, B, H, Lq, d));
-    a.out = tref(fix_unit_strides(out, B, H, Lq, d));
-    a.dout = tref(fix_unit_strides(dout, B, H, Lq, d));
-    a.k = tref(fix_unit_strides(k, B, H, Lk, d));
-    a.v = tref(fix_unit_strides(v, B, H, Lk, d));
+    q = fix_unit_strides(q, B, H, Lq, d);
+    out = fix_unit_strides(out, B, H, Lq, d);
+    dout = fix_unit_strides(dout, B, H, Lq, d);
+    k = fix_unit_strides(k, B, H, Lk, d);
+    v = fix_unit_strides(v, B, H, Lk, d);
+    a.q = tref(q);
+    a.out = tref(out);
+    a.dout = tref(dout);
+    a.k = tref(k);
+    a.v = tref(v);
     a.lse = lse;
     a.D = static_cast<float *>(ws.ptr);
     a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
@@ -929,7 +956,7 @@ int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tens
     a.dk = dk;
     a.dv = dv;
     a.accumulate = accumulate != 0;
-    return ba::launch_attn_bwd(a, g_num_sms[dev], stream);
+    return run_bwd(a, q, k, v, dout, Lq, Lk, dev, stream);
 }
 
 size_t ring_attn_bwd_workspace_size(int B, int H, int T) { return attn_block_bwd_workspace_size(B, H, T); }
@@ -970,11 +997,16 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
     a.kpm_ld = kpm_ld;
     a.am = attn_mask;
     a.am_ld = am_ld;
-    a.q = tref(fix_unit_strides(q, B, H, T, d));
-    a.out = tref(fix_unit_strides(out, B, H, T, d));
-    a.dout = tref(fix_unit_strides(dout, B, H, T, d));
-    a.k = tref(fix_unit_strides(k, B, H, T, d));
-    a.v = tref(fix_unit_strides(v, B, H, T, d));
+    q = fix_unit_strides(q, B, H, T, d);
+    out = fix_unit_strides(out, B, H, T, d);
+    dout = fix_unit_strides(dout, B, H, T, d);
+    k = fix_unit_strides(k, B, H, T, d);
+    v = fix_unit_strides(v, B, H, T, d);
+    a.q = tref(q);
+    a.out = tref(out);
+    a.dout = tref(dout);
+    a.k = tref(k);
+    a.v = tref(v);
     a.lse = lse;
     a.D = static_cast<float *>(ws.ptr);
     a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
@@ -985,7 +1017,7 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
         a.s_begin = 0;
         a.s_end = P;
         a.accumulate = 0;
-        return ba::launch_attn_bwd(a, g_num_sms[dev], stream);
+        return run_bwd(a, q, k, v, dout, T, T, dev, stream);
     }
     // Step-wise, as on the page: step s pairs the queries of rank r with the
     // K/V block of rank (r - s) mod P; dQ accumulates in place and dK / dV
@@ -994,7 +1026,7 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
         a.s_begin = s;
         a.s_end = s + 1;
         a.accumulate = s > 0;
-        if ((rc = ba::launch_attn_bwd(a, g_num_sms[dev], stream))) return rc;
+        if ((rc = run_bwd(a, q, k, v, dout, T, T, dev, stream))) return rc;
     }
     return BA_OK;
 }

@@ -392,20 +392,27 @@ int launch_d(const BwdArgs &a, int n_qt, int n_kt, cudaStream_t s) {
 
 }  // namespace
 
+// D_i = dout_i . out_i for every query row into a.D.
+int launch_bwd_pre(const BwdArgs &a, int num_sms, cudaStream_t s) {
+    const long long q_rows = a.ring ? a.T : a.Lq;
+    const long long warps = (long long)a.B * a.H * q_rows;
+    if (warps == 0) return BA_OK;
+    long long blocks = (warps + 7) / 8;
+    if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+    bwd_pre_kernel<<<(int)blocks, 256, 0, s>>>(a, q_rows);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
 // D = rowsum(dout * out), then dK/dV and dQ.  a.D must hold B*H*rows floats.
 int launch_attn_bwd(const BwdArgs &a, int num_sms, cudaStream_t s) {
     const int BH = a.B * a.H;
     if (BH == 0) return BA_OK;
     if (BH > 65535) return BA_ERR_SHAPE;
-    const long long q_rows = a.ring ? a.T : a.Lq;
     const int n_qt = a.ring ? a.NC * ((a.CL + BT - 1) / BT) : (a.Lq + BT - 1) / BT;
     const int n_kt = a.ring ? a.NC * ((a.CL + BT - 1) / BT) : (a.Lk + BT - 1) / BT;
-    if (q_rows > 0) {
-        const long long warps = (long long)BH * q_rows;
-        long long blocks = (warps + 7) / 8;
-        if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
-        bwd_pre_kernel<<<(int)blocks, 256, 0, s>>>(a, q_rows);
-        if (cudaGetLastError() != cudaSuccess) return BA_ERR_CUDA;
+    {
+        const int rc = launch_bwd_pre(a, num_sms, s);
+        if (rc) return rc;
     }
     switch (a.d) {
         case 16: return launch_d<16>(a, n_qt, n_kt, s);

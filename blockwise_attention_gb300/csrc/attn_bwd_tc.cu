@@ -1,0 +1,682 @@
+// Attention backward on the tensor cores (tcgen05, bf16 inputs, d = 64 / 128).
+//
+// The gradients of "Sequence/context parallelism" (brunomaga), section "Ring
+// Attention", backward pass: with p_ij = exp(scale q_i . k_j - LSE_i) from the
+// saved LSE of the whole row and D_i = dout_i . out_i,
+//   dV_j = sum_i p_ij dout_i,  ds_ij = p_ij (dout_i . v_j - D_i),
+//   dK_j = scale sum_i ds_ij q_i,  dQ_i = scale sum_j ds_ij k_j.
+// Two kernels, no atomics (every output row is written by one CTA):
+//
+// bwd_dkdv_tc_kernel: one CTA per 128-key tile of one (b, h).  K and V of the
+//   tile stay in shared memory; the query tiles that see them stream through a
+//   two-stage ring (Q, dout, and the rows' LSE and D).  Per query tile:
+//     S^T  = K Q^T     (8 MMAs, fp32 into TMEM)
+//     dP^T = V dout^T  (8 MMAs)
+//     the elementwise warps form P^T and dS^T (bf16) over those TMEM columns
+//     dV  += P^T dout  (A = P^T from TMEM, B = dout MN-major)
+//     dK  += dS^T Q    (A = dS^T from TMEM, B = Q MN-major)
+// bwd_dq_tc_kernel: one CTA per 128-row query tile; key tiles stream:
+//     S = Q K^T, dP = dout V^T, dS (bf16) over S, dQ += dS K.
+// Seven products per (query tile, key tile) against the five of the gradient
+// itself: S and dP are formed in both kernels, which is what keeps dQ free of
+// atomics.  The scale is applied to dK and dQ in the epilogues.
+//
+// Roles (256 threads): warp 0 TMA producer (and the LSE / D rows, loaded by its
+// 32 lanes), warp 1 TMEM owner and MMA issuer (converged, one elected lane per
+// instruction), warps 4..7 elementwise + epilogue (thread t owns TMEM lane t).
+// Every mbarrier wait is bounded, as in the forward kernel.
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace ba {
+namespace {
+
+template <int D>
+struct BCfg {
+    static constexpr int NBOX = D / 64;
+    static constexpr int BOX_BYTES = TILE * 128;          // 128 rows x 128 bytes
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES;   // one 128-row tile of one tensor
+    static constexpr int NST = 2;                         // streamed stages
+    static constexpr int RES_OFF = 0;                     // resident pair: R0, R1
+    static constexpr int STG_OFF = 2 * TILE_BYTES;
+    static constexpr int VEC_OFF = 2 * TILE_BYTES;        // within a stage: 128 LSE (log2 units) + 128 D
+    static constexpr int STG_BYTES = 2 * TILE_BYTES + 1024;
+    static constexpr int BAR_OFF = STG_OFF + NST * STG_BYTES;
+    enum { B_RES = 0, B_FULL, B_EMPTY = B_FULL + NST, B_SFULL = B_EMPTY + NST, B_PFULL, B_DONE, B_DRAIN, NBAR };
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort
+    // At least 120 KB, so that one CTA occupies an SM: each CTA allocates all
+    // 512 TMEM columns, and a second one would wait inside tcgen05.alloc.
+    static constexpr int SMEM_USED = MISC_OFF + 16 + 1024;
+    static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, ACC0_COL = 256, ACC1_COL = 256 + D;
+    static constexpr uint32_t TMEM_COLS = 512;
+    // kind::f16, fp32 accumulate, bf16 A and B, N >> 3 at 17, M >> 4 at 24
+    static constexpr uint32_t IDESC_SS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TILE >> 3) << 17) |
+                                         ((uint32_t)(TILE >> 4) << 24);
+    static constexpr uint32_t IDESC_TS = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                         ((uint32_t)(D >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+};
+
+// A 128-row tile of one side with the global position of its first row.
+struct BTile {
+    long long row0;
+    int len;
+    long long pos0;
+    int chunk;
+};
+
+__device__ __forceinline__ BTile btile(const BwdArgs &a, int t, bool is_q) {
+    BTile x;
+    if (!a.ring) {
+        const int L = is_q ? a.Lq : a.Lk;
+        x.row0 = (long long)t * TILE;
+        x.len = min(TILE, L - (int)x.row0);
+        x.pos0 = x.row0 + (is_q ? a.q_off : a.k_off);
+        x.chunk = 0;
+    } else {
+        const int per = (a.CL + TILE - 1) / TILE;
+        x.chunk = t / per;
+        const int r = (t % per) * TILE;
+        x.row0 = (long long)x.chunk * a.CL + r;
+        x.len = min(TILE, a.CL - r);
+        x.pos0 = x.row0;
+    }
+    return x;
+}
+
+__device__ __forceinline__ int n_tiles_side(const BwdArgs &a, bool is_q) {
+    if (a.ring) return a.NC * ((a.CL + TILE - 1) / TILE);
+    return ((is_q ? a.Lq : a.Lk) + TILE - 1) / TILE;
+}
+
+// Walk over the partner tiles of an own tile: the rows of the other side that
+// the covered ring steps pair it with (block mode: the whole other side), cut
+// into 128-row tiles, with causal clipping.  Every role of a CTA runs the same
+// walk.
+struct PWalk {
+    int step, span;
+    long long row, row_end, dpos;
+    bool open;
+};
+
+__device__ __forceinline__ bool pwalk_span(const BwdArgs &a, const BTile &own, bool own_is_key, PWalk &w) {
+    // set [row, row_end) to span `w.span` of step `w.step`; false when the walk is over
+    for (;;) {
+        const int nsteps = a.ring ? a.s_end - a.s_begin : 1;
+        if (w.step >= nsteps) return false;
+        long long r0, r1, dpos;
+        if (!a.ring) {
+            if (w.span > 0) {
+                ++w.step;
+                w.span = 0;
+                continue;
+            }
+            r0 = 0;
+            r1 = own_is_key ? a.Lq : a.Lk;
+            dpos = own_is_key ? a.q_off : a.k_off;
+        } else {
+            const int nsp = a.zigzag ? 2 : 1;
+            if (w.span >= nsp) {
+                ++w.step;
+                w.span = 0;
+                continue;
+            }
+            const int me = !a.zigzag ? own.chunk : (own.chunk < a.P ? own.chunk : 2 * a.P - 1 - own.chunk);
+            const int s = a.s_begin + w.step;
+            // keys of rank src meet the queries of rank (src + s) mod P;
+            // queries of rank r meet the keys of rank (r - s) mod P
+            const int other = own_is_key ? (me + s) % a.P : ((me - s) % a.P + a.P) % a.P;
+            const int c = w.span == 0 ? other : 2 * a.P - 1 - other;
+            r0 = (long long)c * a.CL;
+            r1 = r0 + a.CL;
+            dpos = 0;
+        }
+        if (a.causal) {
+            if (own_is_key) {   // queries before the first key see none of the tile
+                const long long lo = own.pos0 - dpos;
+                if (r0 < lo) r0 = lo;
+            } else {            // keys after the last query are seen by none of it
+                const long long hi = own.pos0 + own.len - dpos;
+                if (r1 > hi) r1 = hi;
+            }
+        }
+        w.row = r0;
+        w.row_end = r1;
+        w.dpos = dpos;
+        if (r0 < r1) return true;
+        ++w.span;
+    }
+}
+
+__device__ __forceinline__ void pwalk_begin(const BwdArgs &a, const BTile &own, bool own_is_key, PWalk &w) {
+    w.step = 0;
+    w.span = 0;
+    w.open = pwalk_span(a, own, own_is_key, w);
+}
+
+// Next partner tile into p; false at the end.
+__device__ __forceinline__ bool pwalk_next(const BwdArgs &a, const BTile &own, bool own_is_key, PWalk &w,
+                                           BTile &p) {
+    while (w.open) {
+        if (w.row < w.row_end) {
+            p.row0 = w.row;
+            p.len = (int)min((long long)TILE, w.row_end - w.row);
+            p.pos0 = w.row + w.dpos;
+            p.chunk = 0;
+            w.row += TILE;
+            return true;
+        }
+        ++w.span;
+        w.open = pwalk_span(a, own, own_is_key, w);
+    }
+    return false;
+}
+
+__device__ __forceinline__ bool bexcluded(const BwdArgs &a, int b, long long qp, long long kp) {
+    if (a.causal && kp > qp) return true;
+    if (a.kpm && a.kpm[b * a.kpm_ld + kp]) return true;
+    if (a.am && a.am[qp * a.am_ld + kp]) return true;
+    return false;
+}
+
+// Common prologue: barriers, TMEM, tensor-map prefetch.  Returns the TMEM base.
+template <int D>
+__device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_t *misc, uint32_t misc_addr,
+                                                 int full_count, const CUtensorMap *m0, const CUtensorMap *m1,
+                                                 const CUtensorMap *m2, const CUtensorMap *m3) {
+    using C = BCfg<D>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_RES), 1);
+        for (int i = 0; i < C::NST; ++i) {
+            mbar_init(bar(C::B_FULL + i), full_count);
+            mbar_init(bar(C::B_EMPTY + i), 1);
+        }
+        mbar_init(bar(C::B_SFULL), 1);
+        mbar_init(bar(C::B_PFULL), 128);
+        mbar_init(bar(C::B_DONE), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
+        misc[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(misc_addr),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m0)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m1)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m2)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m3)) : "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return misc[0];
+}
+
+// 128 rows of one tensor (all its 64-column boxes) at row `row0` of (b, h).
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, long long row0, int h, int b,
+                                         uint32_t bar) {
+    using C = BCfg<D>;
+#pragma unroll
+    for (int bx = 0; bx < C::NBOX; ++bx) tma_load_4d(dst + bx * C::BOX_BYTES, map, bx * 64, (int)row0, h, b, bar);
+}
+
+// The elementwise warps' epilogue: D fp32 columns of one TMEM lane to a global
+// row.  Every lane of the warp executes the (warp-collective) TMEM loads; only
+// lanes with a valid row store.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float *dst, float mul, bool acc, bool valid) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+        if (!valid) continue;
+        float4 *o = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 v = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
+                                   __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
+            if (acc) {
+                const float4 old = o[i];
+                v.x += old.x;
+                v.y += old.y;
+                v.z += old.z;
+                v.w += old.w;
+            }
+            o[i] = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV
+// ---------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dkdv_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_base);
+    const uint32_t bars = base + C::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + C::MISC_OFF + 4);
+    const uint32_t sK = base + C::RES_OFF, sV = sK + C::TILE_BYTES;
+    auto stage = [&](int st) { return base + C::STG_OFF + (uint32_t)st * C::STG_BYTES; };
+    auto vec = [&](int st) {
+        return reinterpret_cast<float *>(gbase + C::STG_OFF + st * C::STG_BYTES + C::VEC_OFF);
+    };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+    const BTile kt = btile(a, blockIdx.x, false);
+    const long long q_rows = a.ring ? a.T : a.Lq;
+    const uint64_t lim = a.wait_limit_ns;
+    const uint32_t tmem = bwd_prologue<D>(bars, misc, base + C::MISC_OFF, 32, &tq, &tk, &tv, &tdo);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (all lanes)
+        bool ok = true;
+        uint32_t fills = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
+            tma_tile<D>(sK, &tk, kt.row0, h, b, bar(C::B_RES));
+            tma_tile<D>(sV, &tv, kt.row0, h, b, bar(C::B_RES));
+        }
+        PWalk pw;
+        pwalk_begin(a, kt, true, pw);
+        BTile pt;
+        while (ok && pwalk_next(a, kt, true, pw, pt)) {
+            const int st = fills % C::NST;
+            const uint32_t use = fills / C::NST;
+            if (use > 0 && !warp_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            float *lse2 = vec(st), *dd = lse2 + TILE;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane * 4 + i;
+                float L = -INFINITY, Dv = 0.f;
+                if (c < pt.len) {
+                    const long long row = (long long)bh * q_rows + pt.row0 + c;
+                    L = a.lse[row];
+                    Dv = a.D[row];
+                }
+                // +inf makes p = exp2(x - lse2) exactly 0 for rows past the tile and rows without keys
+                lse2[c] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+                dd[c] = Dv;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+                tma_tile<D>(stage(st), &tq, pt.row0, h, b, bar(C::B_FULL + st));
+                tma_tile<D>(stage(st) + C::TILE_BYTES, &tdo, pt.row0, h, b, bar(C::B_FULL + st));
+            } else {
+                mbar_arrive(bar(C::B_FULL + st));
+            }
+            ++fills;
+        }
+        if (!ok && lane == 0) {
+            volatile int never = 0;
+            mbar_wait(bar(C::B_RES), 0, &never, nullptr, 200000000ull);
+            for (uint32_t i = 0; i < (uint32_t)C::NST && i < fills; ++i) {
+                const uint32_t last = fills - 1 - i;
+                mbar_wait(bar(C::B_FULL + last % C::NST), (last / C::NST) & 1, &never, nullptr, 200000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (converged)
+        bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
+        const uint64_t kdesc = sdesc(sK, 16, 1024), vdesc = sdesc(sV, 16, 1024);   // K-major A operands
+        uint32_t t = 0;
+        PWalk pw;
+        pwalk_begin(a, kt, true, pw);
+        BTile pt;
+        while (ok && pwalk_next(a, kt, true, pw, pt)) {
+            const int st = t % C::NST;
+            if (!warp_wait(bar(C::B_FULL + st), (t / C::NST) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sQ = stage(st), sDO = stage(st) + C::TILE_BYTES;
+            const uint64_t qk = sdesc(sQ, 16, 1024), dok = sdesc(sDO, 16, 1024);   // K-major B operands
+            // S^T = K Q^T and dP^T = V dout^T (fp32 into TMEM)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::S_COL, kdesc + off, qk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::DP_COL, vdesc + off, dok + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_one(bar(C::B_SFULL));
+            if (!warp_wait(bar(C::B_PFULL), t & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();   // P^T and dS^T were written by the elementwise warps' tcgen05.st
+            const uint64_t don = sdesc(sDO, C::BOX_BYTES, 1024), qn = sdesc(sQ, C::BOX_BYTES, 1024);   // MN-major B
+#pragma unroll
+            for (int kk = 0; kk < TILE / 16; ++kk)
+                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + kk * 8, don + (uint64_t)((kk * 2048) >> 4),
+                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dout
+#pragma unroll
+            for (int kk = 0; kk < TILE / 16; ++kk)
+                mma_ts_one(tmem + C::ACC1_COL, tmem + C::DP_COL + kk * 8, qn + (uint64_t)((kk * 2048) >> 4),
+                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T q
+            mma_commit_one(bar(C::B_EMPTY + st));
+            ++t;
+        }
+        if (ok) {
+            mma_commit_one(bar(C::B_DONE));
+        } else {
+            volatile int never = 0;
+            mma_commit_one(bar(C::B_DRAIN));
+            warp_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ elementwise + epilogue
+        const int j = (warp & 3) * 32 + lane;               // key row of the tile (TMEM lane)
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const bool jvalid = j < kt.len;
+        const long long kp = kt.pos0 + j;
+        const float sl2 = a.scale * 1.4426950408889634f;
+        bool ok = true;
+        uint32_t t = 0;
+        PWalk pw;
+        pwalk_begin(a, kt, true, pw);
+        BTile pt;
+        while (ok && pwalk_next(a, kt, true, pw, pt)) {
+            const int st = t % C::NST;
+            if (!warp_wait(bar(C::B_SFULL), t & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float *lse2 = vec(st), *dd = lse2 + TILE;
+            const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
+                              (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
+            uint32_t pp[TILE / 2], pd[TILE / 2];
+#pragma unroll
+            for (int c = 0; c < TILE / 32; ++c) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
+                tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
+                tmem_wait_ld();
+                float pv[32], dv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = c * 32 + i;
+                    float p = fast_exp2(fmaf(__uint_as_float(rs[i]), sl2, -lse2[col]));
+                    // (columns past the partner tile already give p = 0 through lse2 = +inf;
+                    // they are not looked up in the masks)
+                    if (!full && (!jvalid || col >= pt.len || bexcluded(a, b, pt.pos0 + col, kp))) p = 0.f;
+                    pv[i] = p;
+                    dv[i] = p * (__uint_as_float(rd[i]) - dd[col]);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    pp[c * 16 + i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+                    pd[c * 16 + i] = pack_bf16(dv[2 * i], dv[2 * i + 1]);
+                }
+            }
+            // P^T over the first 64 S^T columns, dS^T over the first 64 dP^T columns
+            tmem_st32(tmem + lane_addr + C::S_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pp[0]));
+            tmem_st32(tmem + lane_addr + C::S_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pp[32]));
+            tmem_st32(tmem + lane_addr + C::DP_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pd[0]));
+            tmem_st32(tmem + lane_addr + C::DP_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pd[32]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+            ++t;
+        }
+        if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {
+            tc_fence_after();
+            const long long row = ((long long)bh * (a.ring ? a.T : a.Lk) + kt.row0 + j) * D;
+            if (t > 0) {   // t is the same for every lane: the TMEM loads below stay warp-collective
+                store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dv + row, 1.f, a.accumulate != 0, jvalid);
+                store_acc_row<D>(tmem + lane_addr + C::ACC1_COL, a.dk + row, a.scale, a.accumulate != 0, jvalid);
+            } else if (jvalid && !a.accumulate) {
+                for (int c = 0; c < D; ++c) a.dv[row + c] = a.dk[row + c] = 0.f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// dQ
+// ---------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dq_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw_base);
+    const uint32_t bars = base + C::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
+    volatile int *abort = reinterpret_cast<volatile int *>(gbase + C::MISC_OFF + 4);
+    const uint32_t sQ = base + C::RES_OFF, sDO = sQ + C::TILE_BYTES;
+    auto stage = [&](int st) { return base + C::STG_OFF + (uint32_t)st * C::STG_BYTES; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+    // heaviest query tiles first under causal masking (the last tiles see the most keys)
+    const BTile qt = btile(a, n_tiles_side(a, true) - 1 - (int)blockIdx.x, true);
+    const long long q_rows = a.ring ? a.T : a.Lq;
+    const uint64_t lim = a.wait_limit_ns;
+    const uint32_t tmem = bwd_prologue<D>(bars, misc, base + C::MISC_OFF, 1, &tq, &tk, &tv, &tdo);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (one lane)
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t fills = 0;
+            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
+            tma_tile<D>(sQ, &tq, qt.row0, h, b, bar(C::B_RES));
+            tma_tile<D>(sDO, &tdo, qt.row0, h, b, bar(C::B_RES));
+            PWalk pw;
+            pwalk_begin(a, qt, false, pw);
+            BTile pt;
+            while (pwalk_next(a, qt, false, pw, pt)) {
+                const int st = fills % C::NST;
+                const uint32_t use = fills / C::NST;
+                if (use > 0 && !mbar_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+                tma_tile<D>(stage(st), &tk, pt.row0, h, b, bar(C::B_FULL + st));
+                tma_tile<D>(stage(st) + C::TILE_BYTES, &tv, pt.row0, h, b, bar(C::B_FULL + st));
+                ++fills;
+            }
+            if (!ok) {
+                volatile int never = 0;
+                mbar_wait(bar(C::B_RES), 0, &never, nullptr, 200000000ull);
+                for (uint32_t i = 0; i < (uint32_t)C::NST && i < fills; ++i) {
+                    const uint32_t last = fills - 1 - i;
+                    mbar_wait(bar(C::B_FULL + last % C::NST), (last / C::NST) & 1, &never, nullptr, 200000000ull);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (converged)
+        bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
+        const uint64_t qdesc = sdesc(sQ, 16, 1024), dodesc = sdesc(sDO, 16, 1024);   // K-major A operands
+        uint32_t t = 0;
+        PWalk pw;
+        pwalk_begin(a, qt, false, pw);
+        BTile pt;
+        while (ok && pwalk_next(a, qt, false, pw, pt)) {
+            const int st = t % C::NST;
+            if (!warp_wait(bar(C::B_FULL + st), (t / C::NST) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sK = stage(st), sV = stage(st) + C::TILE_BYTES;
+            const uint64_t kk_ = sdesc(sK, 16, 1024), vk = sdesc(sV, 16, 1024);   // K-major B operands
+            // S = Q K^T and dP = dout V^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::S_COL, qdesc + off, kk_ + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::DP_COL, dodesc + off, vk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_one(bar(C::B_SFULL));
+            if (!warp_wait(bar(C::B_PFULL), t & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();   // dS was written by the elementwise warps' tcgen05.st
+            const uint64_t kn = sdesc(sK, C::BOX_BYTES, 1024);   // K as the MN-major B operand
+#pragma unroll
+            for (int kk = 0; kk < TILE / 16; ++kk)
+                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + kk * 8, kn + (uint64_t)((kk * 2048) >> 4),
+                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dQ += dS K
+            mma_commit_one(bar(C::B_EMPTY + st));
+            ++t;
+        }
+        if (ok) {
+            mma_commit_one(bar(C::B_DONE));
+        } else {
+            volatile int never = 0;
+            mma_commit_one(bar(C::B_DRAIN));
+            warp_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ elementwise + epilogue
+        const int i = (warp & 3) * 32 + lane;               // query row of the tile (TMEM lane)
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const bool ivalid = i < qt.len;
+        const long long qp = qt.pos0 + i;
+        const float sl2 = a.scale * 1.4426950408889634f;
+        float lse2 = INFINITY, Dv = 0.f;
+        if (ivalid) {
+            const long long row = (long long)bh * q_rows + qt.row0 + i;
+            const float L = a.lse[row];
+            lse2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+            Dv = a.D[row];
+        }
+        bool ok = true;
+        uint32_t t = 0;
+        PWalk pw;
+        pwalk_begin(a, qt, false, pw);
+        BTile pt;
+        while (ok && pwalk_next(a, qt, false, pw, pt)) {
+            if (!warp_wait(bar(C::B_SFULL), t & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
+                              (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
+            uint32_t pd[TILE / 2];
+#pragma unroll
+            for (int c = 0; c < TILE / 32; ++c) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
+                tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
+                tmem_wait_ld();
+                float dv[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int col = c * 32 + k;
+                    float p = fast_exp2(fmaf(__uint_as_float(rs[k]), sl2, -lse2));
+                    if (!full && (!ivalid || col >= pt.len || bexcluded(a, b, qp, pt.pos0 + col))) p = 0.f;
+                    dv[k] = p * (__uint_as_float(rd[k]) - Dv);
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) pd[c * 16 + k] = pack_bf16(dv[2 * k], dv[2 * k + 1]);
+            }
+            tmem_st32(tmem + lane_addr + C::S_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pd[0]));
+            tmem_st32(tmem + lane_addr + C::S_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pd[32]));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(C::B_PFULL));
+            ++t;
+        }
+        if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {
+            tc_fence_after();
+            const long long row = ((long long)bh * q_rows + qt.row0 + i) * D;
+            if (t > 0)   // uniform: the TMEM loads stay warp-collective
+                store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dq + row, a.scale, a.accumulate != 0, ivalid);
+            else if (ivalid && !a.accumulate)
+                for (int c = 0; c < D; ++c) a.dq[row + c] = 0.f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+}
+
+template <int D>
+int launch_bwd_tc_d(const BwdArgs &a, const BwdMaps &m, cudaStream_t s) {
+    using C = BCfg<D>;
+    static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
+    if (cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+            cudaSuccess)
+        return BA_ERR_CUDA;
+    const int BH = a.B * a.H;
+    const int n_kt = a.ring ? a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lk + TILE - 1) / TILE;
+    const int n_qt = a.ring ? a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lq + TILE - 1) / TILE;
+    if (n_kt > 0) bwd_dkdv_tc_kernel<D><<<dim3(n_kt, BH), 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    if (n_qt > 0) bwd_dq_tc_kernel<D><<<dim3(n_qt, BH), 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int dtype, int d) { return dtype == BA_BF16 && (d == 64 || d == 128); }
+
+// D pre-pass, then the dK/dV and dQ tensor-core kernels.
+int launch_attn_bwd_tc(const BwdArgs &a, const BwdMaps &m, int num_sms, cudaStream_t s) {
+    const int BH = a.B * a.H;
+    if (BH == 0) return BA_OK;
+    if (BH > 65535) return BA_ERR_SHAPE;
+    int rc = launch_bwd_pre(a, num_sms, s);
+    if (rc) return rc;
+    if (a.d == 128) return launch_bwd_tc_d<128>(a, m, s);
+    if (a.d == 64) return launch_bwd_tc_d<64>(a, m, s);
+    return BA_ERR_SHAPE;
+}
+
+}  // namespace ba

@@ -55,9 +55,19 @@ struct BwdArgs {
     float scale;
     float *dq, *dk, *dv;                 // fp32 (B, H, L, d) contiguous
     int accumulate;                      // add into dq / dk / dv instead of overwriting
+    unsigned *err;                       // device error word (tensor-core kernels)
+    unsigned long long wait_limit_ns;    // bounded-wait limit (tensor-core kernels)
+};
+
+// TMA descriptors of q, k, v and dout for the tensor-core backward.
+struct BwdMaps {
+    CUtensorMap q, k, v, dout;
 };
 
 int launch_attn_bwd(const BwdArgs &a, int num_sms, cudaStream_t s);
+int launch_bwd_pre(const BwdArgs &a, int num_sms, cudaStream_t s);
+bool bwd_tc_supported(int dtype, int d);
+int launch_attn_bwd_tc(const BwdArgs &a, const BwdMaps &m, int num_sms, cudaStream_t s);
 
 // One Ulysses exchange: the token-split stacked array (P, H, B, Tl, d),
 // contiguous, against a strided (B, H, T = P Tl, d) view of the head side.

@@ -179,6 +179,45 @@ __device__ __forceinline__ bool bexcluded(const BwdArgs &a, int b, long long qp,
     return false;
 }
 
+// Visibility of 32 pairs as a bit mask (bit i: pair i is kept), for the tiles
+// that need exclusions.  Kept out of line: inlined into the unrolled elementwise
+// loops it made them too large for the instruction cache.
+// Key fixed (dK/dV kernel): queries q0 + i, i < 32, of which the first n exist.
+__device__ __noinline__ uint32_t keep_bits_queries(const BwdArgs &a, int b, long long q0, int n, long long kp,
+                                                   bool kvalid) {
+    uint32_t m = 0;
+    if (!kvalid) return 0;
+    for (int i = 0; i < 32 && i < n; ++i)
+        if (!bexcluded(a, b, q0 + i, kp)) m |= 1u << i;
+    return m;
+}
+// Query fixed (dQ kernel): keys k0 + i, i < 32, of which the first n exist.
+__device__ __noinline__ uint32_t keep_bits_keys(const BwdArgs &a, int b, long long qp, bool qvalid, long long k0,
+                                                int n) {
+    uint32_t m = 0;
+    if (!qvalid) return 0;
+    for (int i = 0; i < 32 && i < n; ++i)
+        if (!bexcluded(a, b, qp, k0 + i)) m |= 1u << i;
+    return m;
+}
+
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// Four consecutive floats of shared memory (16-byte aligned address).
+__device__ __forceinline__ float4 lds4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr));
+    return v;
+}
+
 // Common prologue: barriers, TMEM, tensor-map prefetch.  Returns the TMEM base.
 template <int D>
 __device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_t *misc, uint32_t misc_addr,
@@ -315,8 +354,9 @@ __global__ void __launch_bounds__(256, 1)
                     L = a.lse[row];
                     Dv = a.D[row];
                 }
-                // +inf makes p = exp2(x - lse2) exactly 0 for rows past the tile and rows without keys
-                lse2[c] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+                // -LSE in log2 units; -inf makes p = exp2(x + nlse2) exactly 0 for rows
+                // past the tile and rows without keys
+                lse2[c] = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
                 dd[c] = Dv;
             }
             if (lane == 0) {
@@ -409,38 +449,42 @@ __global__ void __launch_bounds__(256, 1)
                 break;
             }
             tc_fence_after();
-            const float *lse2 = vec(st), *dd = lse2 + TILE;
+            const uint32_t s_nlse = smem_u32(vec(st)), s_dd = s_nlse + TILE * 4;   // -LSE log2 units, D
             const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
-            uint32_t pp[TILE / 2], pd[TILE / 2];
 #pragma unroll
             for (int c = 0; c < TILE / 32; ++c) {
                 uint32_t rs[32], rd[32];
                 tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
                 tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
                 tmem_wait_ld();
-                float pv[32], dv[32];
+                const uint32_t keep =
+                    full ? 0xffffffffu
+                         : keep_bits_queries(a, b, pt.pos0 + c * 32, pt.len - c * 32, kp, jvalid);
+                uint32_t pp[16], pd[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = c * 32 + i;
-                    float p = fast_exp2(fmaf(__uint_as_float(rs[i]), sl2, -lse2[col]));
-                    // (columns past the partner tile already give p = 0 through lse2 = +inf;
-                    // they are not looked up in the masks)
-                    if (!full && (!jvalid || col >= pt.len || bexcluded(a, b, pt.pos0 + col, kp))) p = 0.f;
-                    pv[i] = p;
-                    dv[i] = p * (__uint_as_float(rd[i]) - dd[col]);
-                }
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 nl = lds4(s_nlse + (c * 32 + q4 * 4) * 4);
+                    const float4 d4 = lds4(s_dd + (c * 32 + q4 * 4) * 4);
+                    const float nlv[4] = {nl.x, nl.y, nl.z, nl.w}, ddv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dv[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    pp[c * 16 + i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
-                    pd[c * 16 + i] = pack_bf16(dv[2 * i], dv[2 * i + 1]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = q4 * 4 + e;
+                        float p = fast_exp2(fmaf(__uint_as_float(rs[i]), sl2, nlv[e]));
+                        p = (keep >> i) & 1u ? p : 0.f;   // columns past the partner tile are never kept
+                        pv[e] = p;
+                        dv[e] = p * (__uint_as_float(rd[i]) - ddv[e]);
+                    }
+                    pp[q4 * 2] = pack_bf16(pv[0], pv[1]);
+                    pp[q4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
+                    pd[q4 * 2] = pack_bf16(dv[0], dv[1]);
+                    pd[q4 * 2 + 1] = pack_bf16(dv[2], dv[3]);
                 }
+                // P^T / dS^T of these 32 queries into 16 columns the earlier chunks have read
+                tmem_st16(tmem + lane_addr + C::S_COL + c * 16, pp);
+                tmem_st16(tmem + lane_addr + C::DP_COL + c * 16, pd);
             }
-            // P^T over the first 64 S^T columns, dS^T over the first 64 dP^T columns
-            tmem_st32(tmem + lane_addr + C::S_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pp[0]));
-            tmem_st32(tmem + lane_addr + C::S_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pp[32]));
-            tmem_st32(tmem + lane_addr + C::DP_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pd[0]));
-            tmem_st32(tmem + lane_addr + C::DP_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pd[32]));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL));
@@ -583,11 +627,11 @@ __global__ void __launch_bounds__(256, 1)
         const bool ivalid = i < qt.len;
         const long long qp = qt.pos0 + i;
         const float sl2 = a.scale * 1.4426950408889634f;
-        float lse2 = INFINITY, Dv = 0.f;
+        float nlse2 = -INFINITY, Dv = 0.f;   // -LSE in log2 units (-inf: p = 0)
         if (ivalid) {
             const long long row = (long long)bh * q_rows + qt.row0 + i;
             const float L = a.lse[row];
-            lse2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+            nlse2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
             Dv = a.D[row];
         }
         bool ok = true;
@@ -603,26 +647,30 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
             const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
-            uint32_t pd[TILE / 2];
 #pragma unroll
             for (int c = 0; c < TILE / 32; ++c) {
                 uint32_t rs[32], rd[32];
                 tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
                 tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
                 tmem_wait_ld();
-                float dv[32];
+                const uint32_t keep =
+                    full ? 0xffffffffu : keep_bits_keys(a, b, qp, ivalid, pt.pos0 + c * 32, pt.len - c * 32);
+                uint32_t pd[16];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int col = c * 32 + k;
-                    float p = fast_exp2(fmaf(__uint_as_float(rs[k]), sl2, -lse2));
-                    if (!full && (!ivalid || col >= pt.len || bexcluded(a, b, qp, pt.pos0 + col))) p = 0.f;
-                    dv[k] = p * (__uint_as_float(rd[k]) - Dv);
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    float dv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = 2 * k2 + e;
+                        float p = fast_exp2(fmaf(__uint_as_float(rs[k]), sl2, nlse2));
+                        p = (keep >> k) & 1u ? p : 0.f;
+                        dv[e] = p * (__uint_as_float(rd[k]) - Dv);
+                    }
+                    pd[k2] = pack_bf16(dv[0], dv[1]);
                 }
-#pragma unroll
-                for (int k = 0; k < 16; ++k) pd[c * 16 + k] = pack_bf16(dv[2 * k], dv[2 * k + 1]);
+                // dS of these 32 keys into 16 columns the earlier chunks have read
+                tmem_st16(tmem + lane_addr + C::S_COL + c * 16, pd);
             }
-            tmem_st32(tmem + lane_addr + C::S_COL, *reinterpret_cast<const uint32_t(*)[32]>(&pd[0]));
-            tmem_st32(tmem + lane_addr + C::S_COL + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pd[32]));
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(C::B_PFULL));

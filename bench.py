@@ -485,7 +485,21 @@ def backward_arm(args, w, rank, world, local_rank):
         return
     value = world * flops / (ms * 1e-3) / 1e12
     sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
-    peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    tensor_path = w.torch_dtype == torch.bfloat16 and w.d in (64, 128)
+    if tensor_path:
+        peaks, src = load_peaks()
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        roof = {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                "traffic": None, "kernel": "bwd_dkdv_tc_kernel + bwd_dq_tc_kernel",
+                "peak_source": f"{src} bf16_tflops_sustained; the kernels execute 14*d FLOP per pair (QK^T and "
+                               f"dout V^T are formed in both) against the 10*d counted",
+                "executed_frac": 1.4 * value / peak}
+    else:
+        peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
+                "traffic": None, "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x sampled SM clock; the kernels "
+                               "execute 14*d FLOP per pair (scores and dout V^T in both)"}
     steps_per = 1 if args.mode == "fused" else w.P
     cpu = None
     if not args.no_cpu:
@@ -503,17 +517,16 @@ def backward_arm(args, w, rank, world, local_rank):
                          f"{cpairs} visible pairs in {dt:.2f} s (one thread per head)"}
     line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": w.P,
                        "partition": w.partition, "causal": w.causal, "mode": args.mode, "direction": "backward",
                        "visible_pairs": pairs, "flops_per_step": flops,
                        "l2": "inputs larger than the 129 MB L2; no flush"},
-            "roofline": {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s",
-                         "frac": value / peak, "traffic": None, "kernel": "bwd_dkdv_kernel + bwd_dq_kernel",
-                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x sampled SM clock; the "
-                                        "kernels execute 14*d FLOP per pair (scores and dout V^T in both)"},
+            "roofline": roof,
             "cpu_baseline": cpu, "e2e": None, "clocks": clocks,
             "gpu_launches": 3 * steps_per * args.steps}
+    if not tensor_path:
+        line["dtype"] = "f32"
     print(json.dumps(line), flush=True)
 
 

@@ -1,37 +1,43 @@
 // Tensor-core attention kernel for sm_103a (bf16 Q/K/V, head dim 64 or 128).
 //
-// Persistent CTAs (one per SM) take work items = (query tile of 128 rows,
-// batch item, head), claimed one at a time from a launch-wide counter in
-// heaviest-first order (or dealt round-robin when no counter is given).  For each item the query tile stays resident in shared
-// memory while the key tiles of its walk arrive in ring order; every tile is
-// folded into a running (row max, denominator, weighted sum) that is rescaled
-// to the new maximum, never added or averaged (brunomaga "Improving numerical
-// stability"; llm-systems "Circulate K/V blocks with Ring").
+// Persistent CTAs (one per SM) take work items = (pair of adjacent query tiles
+// of 128 rows, batch item, head), claimed one at a time from a launch-wide
+// counter in heaviest-first order (or dealt round-robin when no counter is
+// given).  The two query tiles stay resident in shared memory and share every
+// key / value tile of their walk, which arrives in ring order; each tile is
+// folded into a running (row max, denominator, weighted sum) per row that is
+// rescaled to the new maximum, never added or averaged (brunomaga "Improving
+// numerical stability"; llm-systems "Circulate K/V blocks with Ring").
 //
-// Roles (256 threads):
-//   warp 0      TMA producer: Q tile, then K and V tiles into two stage rings
-//               (128B-swizzled boxes of 64 columns x 128 rows); K of tile j is
-//               issued before V of tile j - 1.
-//   warp 1      owns TMEM (512 columns) and issues tcgen05.mma from one thread:
-//               S = Q K^T (A, B from shared memory, fp32 accumulate in TMEM),
-//               O += P V (A = P from TMEM, B = V from shared memory).
-//   warps 4..7  softmax: thread t owns query row t (TMEM lane t).  Reads S,
-//               applies scale and exclusions, updates (m, l), writes P (bf16)
-//               to TMEM, rescales O when the row maximum grows by more than
-//               2^8, and at the end normalises O and stores out / lse.
-//   warps 2..3  idle.
-// S has three buffers and PV runs two tiles behind QK: QK(j+1) and QK(j+2)
-// are computed while the softmax works on tile j, so three tiles are in
-// flight between the tensor pipe and the softmax.  P(j) (bf16, 64 columns) is
-// written over the S buffer it was computed from; QK(j+3), the next writer of
-// that buffer, is issued after PV(j), and the tensor pipe executes in issue
-// order.  K stages are released when their QK completes, V stages when their
-// PV completes.
+// Roles (320 threads, ten warps):
+//   warp 0      TMA producer: both Q tiles, then K and V tiles into two stage
+//               rings (128B-swizzled boxes of 64 columns x 128 rows); K of tile
+//               j is issued before V of tile j - 1.  It also claims the items
+//               and describes every key tile for the softmax warps.
+//   warp 1      owns TMEM (512 columns) and issues tcgen05.mma, one elected
+//               lane per instruction: S_x = Q_x K^T (A, B from shared memory,
+//               fp32 accumulate in TMEM) and O_x += P_x V (A = P_x from TMEM).
+//   warps 2..5  softmax group 0 (query tile 0), warps 6..9 softmax group 1
+//               (query tile 1): thread t of a group owns row t of its tile
+//               (TMEM lane t; warp w reaches lanes 32 (w % 4) .. + 31).  Reads
+//               S_x, applies scale and exclusions, takes the row maximum,
+//               updates (m, l), writes P_x (bf16) over S_x, rescales O_x when the
+//               row maximum grows by more than 2^8, and at the end normalises O_x
+//               and stores out / lse.  Ten warps leave 168 registers a thread:
+//               the 128 scores of a row stay in registers, the probabilities go
+//               to TMEM 32 keys at a time.
+// Ping-pong: per key tile j the MMA warp issues PV_0(j), QK_0(j+1), PV_1(j),
+// QK_1(j+1).  While group 0 works on S_0(j+1) the tensor pipe runs the
+// products of group 1, and the other way round, so the softmax of one group
+// hides under the products of the other, and each K / V tile brought in from
+// L2 serves 256 query rows.  P_x(j) is written over the S_x columns it was
+// computed from; QK_x(j+1), the next writer of S_x, is issued after PV_x(j),
+// and the tensor pipe executes in issue order.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) S2 [256,384) O [384,384+D).
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [256+D,256+2D).
 //
 // The producer passes each claimed item (index, key-tile count) to the MMA
-// thread and the softmax warps through a two-slot ring (ITEM_FULL / ITEM_EMPTY).
+// warp and the softmax warps through a two-slot ring (ITEM_FULL / ITEM_EMPTY).
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // BA_ERR_TIMEOUT in the error word, drains its outstanding copies and MMAs
@@ -50,40 +56,42 @@ struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
     static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
     static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
-    // One K stage and one V stage per S buffer: tile j uses K stage, V stage
-    // and S buffer j % 3, so the S_FULL commit of QK(j) also frees K stage
-    // j % 3 and the PV_DONE commit of PV(j) frees V stage j % 3.
-    static constexpr int NSB = 3;                  // S buffers in TMEM
-    static constexpr int KS = NSB;                 // K stages
-    static constexpr int VS = NSB;                 // V stages
+    static constexpr int KS = D == 128 ? 2 : 3;    // K stages
+    static constexpr int VS = KS;                  // V stages
     static constexpr int TIR = 16;                 // key-tile description ring (power of two)
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = TILE_BYTES;
+    static constexpr int Q_OFF = 0;                // query tile x at Q_OFF + x * TILE_BYTES
+    static constexpr int K_OFF = 2 * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
     enum {
         B_QFULL = 0,
         B_QEMPTY,
         B_KFULL,
-        B_VFULL = B_KFULL + KS,
-        B_SFULL = B_VFULL + VS,     // QK(j) complete: S ready, K stage j % 3 free
-        B_PFULL = B_SFULL + NSB,
-        B_PVDONE = B_PFULL + NSB,   // PV(j) complete: V stage j % 3 free, O may be rescaled
-        B_OFULL = B_PVDONE + NSB,
-        B_OEMPTY,
-        B_DRAIN,
+        B_KEMPTY = B_KFULL + KS,     // QK_0(j) and QK_1(j) complete: K stage free
+        B_VFULL = B_KEMPTY + KS,
+        B_VEMPTY = B_VFULL + VS,     // PV_0(j) and PV_1(j) complete: V stage free
+        B_SFULL = B_VEMPTY + VS,     // [x]: QK_x complete
+        B_PFULL = B_SFULL + 2,       // [x]: P_x stored by group x (128 arrivals)
+        B_PVDONE = B_PFULL + 2,      // [x]: PV_x complete (O_x may be rescaled)
+        B_OFULL = B_PVDONE + 2,      // [x]: the item's last PV_x complete
+        B_OEMPTY = B_OFULL + 2,      // [x]: group x has read O_x out (128 arrivals)
+        B_DRAIN = B_OEMPTY + 2,
         B_ITEMFULL,
         B_ITEMEMPTY = B_ITEMFULL + 2,
         NBAR = B_ITEMEMPTY + 2
     };
     // [0] tmem base, [1] abort, [2..3] item key tiles, [4..5] item index (by item parity)
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-    // TIR x {global position, len | class << 16, tile sequence number + 1, unused}
+    // TIR x {global position, len | class0 << 16 | class1 << 20, tile sequence number + 1, unused}
     static constexpr int TI_OFF = MISC_OFF + 32;
-    static constexpr int SMEM_BYTES = TI_OFF + TIR * 16 + 1024;  // + slack to align the base to 1 KB
-    static constexpr uint32_t S_COL = 0;     // S buffer b at S_COL + 128 b; P over its first 64 columns
-    static constexpr uint32_t O_COL = 384;
+    static constexpr int SMEM_USED = TI_OFF + TIR * 16 + 1024;   // + slack to align the base to 1 KB
+    // At least 120 KB, so that one CTA occupies an SM: each CTA allocates all
+    // 512 TMEM columns, and a second one would wait inside tcgen05.alloc.
+    static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+    static constexpr uint32_t S_COL = 0;           // S_x at S_COL + 128 x; P_x over its first 64 columns
+    static constexpr uint32_t O_COL = 256;         // O_x at O_COL + D x
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 320;
     // Instruction descriptors (kind::f16): D fp32 (bits 4-5 = 1), A and B
     // bf16 (bits 7-9, 10-12 = 1), B major bit 16 (0 = K-major, 1 = MN-major),
     // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
@@ -93,9 +101,9 @@ struct Cfg {
                                          ((uint32_t)(D >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
 };
 
-// 32 bytes of an exclusion mask (1 = excluded) starting at p, of which the
-// first n are meaningful, applied to s[0..31].
-__device__ __forceinline__ void mask_bytes(const uint8_t *p, int n, float *s) {
+// 32 bits of an exclusion mask (1 = excluded, one byte per key) starting at p,
+// of which the first n are meaningful; bit i set when byte i is nonzero.
+__device__ __forceinline__ uint32_t excl_bits(const uint8_t *p, int n) {
     uint32_t w[8];
     if (n >= 32 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
         const uint4 a = __ldg(reinterpret_cast<const uint4 *>(p));
@@ -103,31 +111,145 @@ __device__ __forceinline__ void mask_bytes(const uint8_t *p, int n, float *s) {
         w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
         w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     } else {
-#pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < n) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
+        for (int i = 0; i < 32 && i < n; ++i) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
     }
+    uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-        if ((w[i >> 2] >> (8 * (i & 3))) & 0xffu) s[i] = -INFINITY;
+        if ((w[i >> 2] >> (8 * (i & 3))) & 0xffu) m |= 1u << i;
+    return m;
 }
 
-// Exclusions of keys [c0, c0 + 32) of key tile kt for the query at global
-// position qpos: past the tile end, causal future, key padding, attn_mask.
-__device__ __forceinline__ void mask_chunk(const Geom &g, int b, long long qpos, bool row_valid, const KTile &kt,
-                                           int c0, float *s) {
-    const long long diag = qpos - kt.pos0;   // key j lies in the future when j > diag
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int j = c0 + i;
-        if (j >= kt.len || (g.causal && j > diag)) s[i] = -INFINITY;
+// Keys [c0, c0 + 32) of key tile kt that the query at global position qpos
+// may see (bit i for key c0 + i): inside the tile, not in the causal future,
+// not padded, not forbidden by attn_mask.  Out of line: it runs on PARTIAL
+// tiles only, and inlined into the softmax loop its registers and code sat
+// beside the 128 scores of every tile.
+__device__ __noinline__ uint32_t keep_bits(const Geom &g, int b, long long qpos, bool row_valid, long long kpos0,
+                                           int klen, int c0) {
+    const int n = klen - c0;
+    if (n <= 0) return 0u;
+    uint32_t m = n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+    if (g.causal) {
+        const long long lim = qpos - kpos0 - c0;   // key c0 + i lies in the future when i > lim
+        if (lim < 0) return 0u;
+        if (lim < 31) m &= (2u << lim) - 1u;
     }
-    const int n = kt.len - c0;
-    if (!row_valid || n <= 0) return;
-    if (g.kpm) mask_bytes(g.kpm + b * g.kpm_ld + kt.pos0 + c0, n, s);
-    if (g.am) mask_bytes(g.am + qpos * g.am_ld + kt.pos0 + c0, n, s);
+    if (!row_valid) return m;   // rows past the tile end are never stored; their mask rows may not exist
+    if (g.kpm) m &= ~excl_bits(g.kpm + b * g.kpm_ld + kpos0 + c0, n);
+    if (g.am) m &= ~excl_bits(g.am + qpos * g.am_ld + kpos0 + c0, n);
+    return m;
+}
+
+// ----------------------------------------------------------------------------
+// Pairs of query tiles
+// ----------------------------------------------------------------------------
+//
+// The unit of work is a pair of adjacent query tiles of one chunk (ring mode)
+// or of the block: tiles 2i and 2i + 1 of the chunk; when the chunk has an odd
+// number of tiles its last pair holds one tile.  The two tiles cover
+// consecutive positions, so the pair's key walk is the walk of the 256-row span
+// that covers both; each key tile of it carries one class per tile (a tile that
+// only the second query tile sees is EMPTY for the first, whose rows then see
+// no key in it).
+
+struct QPair {
+    QTile q0, q1;    // q1.len == 0 when the pair holds one tile
+    QTile span;      // both tiles as one query range (walk geometry)
+};
+
+__host__ __device__ inline int pairs_per_chunk(const Geom &g) {
+    const int per = g.ring ? g.nqt_pc : g.n_qtiles;
+    return (per + 1) / 2;
+}
+
+// Pairs per (b, h).
+__host__ __device__ inline int n_pairs(const Geom &g) {
+    return (g.ring ? g.NC : 1) * pairs_per_chunk(g);
+}
+
+// Work item w -> pair.  Items are grouped by heads_per_group (b, h) pairs so
+// that concurrently running CTAs share K/V in L2; within a group the pairs
+// come heaviest first under causal masking (latest positions).
+__device__ inline QPair work_pair(const Geom &g, int w) {
+    const int BH = g.B * g.H, G = g.heads_per_group, np = n_pairs(g);
+    const int per_group = G * np;
+    const int grp = w / per_group, rem = w % per_group;
+    const int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
+    const int pi = rem / g_heads, bh = grp * G + rem % g_heads;
+    const int pg = g.causal ? np - 1 - pi : pi;
+    const int ppc = pairs_per_chunk(g), per = g.ring ? g.nqt_pc : g.n_qtiles;
+    const int c = pg / ppc, i = pg % ppc;
+    const int b = bh / g.H, h = bh % g.H;
+    QPair p;
+    p.q0 = q_tile(g, c * per + 2 * i, b, h);
+    if (2 * i + 1 < per) {
+        p.q1 = q_tile(g, c * per + 2 * i + 1, b, h);
+    } else {
+        p.q1 = p.q0;
+        p.q1.len = 0;
+    }
+    p.span = p.q0;
+    p.span.len = p.q0.len + p.q1.len;
+    return p;
+}
+
+// Next key tile of the pair's walk that one of its query tiles sees, with the
+// class for each (c1 = EMPTY when the pair holds one tile); false at the end.
+__device__ __forceinline__ bool pair_next(const Geom &g, const QPair &p, KWalk &w, KTile &k, int &c0, int &c1) {
+    const int q0_last = (int)p.q0.pos0 + p.q0.len - 1;
+    const bool has1 = p.q1.len > 0;
+    for (;;) {
+        if (w.row >= w.chunk_end) {
+            if (!kwalk_next_chunk(g, w)) return false;
+            continue;
+        }
+        const int row = w.row;
+        const int pos = row + w.pos_off;
+        const int rem = w.chunk_end - row;
+        k.row0 = row;
+        k.len = rem < TILE ? rem : TILE;
+        k.pos0 = pos;
+        k.idx = w.idx;
+        w.row = row + TILE;
+        ++w.idx;
+        if (g.cls) {
+            const int8_t *m = g.cls + ((long long)p.q0.b * g.n_qtiles + p.q0.g) * g.n_ktiles + k.idx;
+            c0 = m[0];
+            c1 = has1 ? m[g.n_ktiles] : BA_TILE_EMPTY;
+            if (c0 == BA_TILE_EMPTY && c1 == BA_TILE_EMPTY) continue;
+            return true;
+        }
+        if (g.causal) {
+            if (pos > w.q_last) {          // this and the rest of the chunk lie in the future of both
+                w.row = w.chunk_end;
+                continue;
+            }
+            const int k_last = pos + k.len - 1;
+            c0 = pos > q0_last ? BA_TILE_EMPTY : (k_last <= (int)p.q0.pos0 ? BA_TILE_FULL : BA_TILE_PARTIAL);
+            c1 = !has1 ? BA_TILE_EMPTY : (k_last <= (int)p.q1.pos0 ? BA_TILE_FULL : BA_TILE_PARTIAL);
+        } else {
+            c0 = BA_TILE_FULL;
+            c1 = has1 ? BA_TILE_FULL : BA_TILE_EMPTY;
+        }
+        if (g.kpm || g.am) {   // masks need predicates
+            if (c0 == BA_TILE_FULL) c0 = BA_TILE_PARTIAL;
+            if (c1 == BA_TILE_FULL) c1 = BA_TILE_PARTIAL;
+        }
+        return true;
+    }
+}
+
+// Number of key tiles pair_next yields for pair p.
+__device__ inline int pair_count(const Geom &g, const QPair &p) {
+    if (!g.cls) return kwalk_count(g, p.span);   // the span's walk: both tiles see a tile the span sees
+    KWalk w;
+    kwalk_begin(g, p.span, w);
+    KTile k;
+    int c0, c1, n = 0;
+    while (pair_next(g, p, w, k, c0, c1)) ++n;
+    return n;
 }
 
 // ----------------------------------------------------------------------------
@@ -135,7 +257,7 @@ __device__ __forceinline__ void mask_chunk(const Geom &g, int b, long long qpos,
 // ----------------------------------------------------------------------------
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
     using C = Cfg<D>;
@@ -158,19 +280,25 @@ __global__ void __launch_bounds__(256, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_QFULL), 1);
         mbar_init(bar(C::B_QEMPTY), 1);
-        for (int i = 0; i < C::KS; ++i) mbar_init(bar(C::B_KFULL + i), 1);
-        for (int i = 0; i < C::VS; ++i) mbar_init(bar(C::B_VFULL + i), 1);
-        for (int i = 0; i < C::NSB; ++i) {
-            mbar_init(bar(C::B_SFULL + i), 1);
-            mbar_init(bar(C::B_PFULL + i), 128);
-            mbar_init(bar(C::B_PVDONE + i), 1);
+        for (int i = 0; i < C::KS; ++i) {
+            mbar_init(bar(C::B_KFULL + i), 1);
+            mbar_init(bar(C::B_KEMPTY + i), 1);
         }
-        mbar_init(bar(C::B_OFULL), 1);
-        mbar_init(bar(C::B_OEMPTY), 128);
+        for (int i = 0; i < C::VS; ++i) {
+            mbar_init(bar(C::B_VFULL + i), 1);
+            mbar_init(bar(C::B_VEMPTY + i), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_SFULL + x), 1);
+            mbar_init(bar(C::B_PFULL + x), 128);
+            mbar_init(bar(C::B_PVDONE + x), 1);
+            mbar_init(bar(C::B_OFULL + x), 1);
+            mbar_init(bar(C::B_OEMPTY + x), 128);
+        }
         mbar_init(bar(C::B_DRAIN), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::B_ITEMFULL + i), 1);
-            mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 4);   // MMA warp + one lane per softmax warp
+            mbar_init(bar(C::B_ITEMEMPTY + i), 1 + 8);   // MMA warp + one lane per softmax warp
         }
         for (int i = 0; i < C::TIR; ++i) tinfo[4 * i + 2] = 0xffffffffu;   // no tile yet
         misc[1] = 0;
@@ -192,9 +320,16 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = misc[0];
+    // A CTA that holds all 512 TMEM columns holds them from column 0, so the
+    // TMEM addresses below are compile-time constants (which keeps the MMA issue
+    // on the uniform datapath).  Any other base is reported through the error
+    // word and nothing runs.
+    const uint32_t tmem_base = misc[0];
+    constexpr uint32_t tmem = 0u;
 
-    if (warp == 0) {
+    if (tmem_base != 0u) {
+        if (threadIdx.x == 0) atomicOr(a.err, ERR_TIMEOUT_BIT);
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             uint32_t kfill = 0, vfill = 0, qfills = 0, it_local = 0;
@@ -204,8 +339,9 @@ __global__ void __launch_bounds__(256, 1)
             // out of work; without a counter they are dealt round-robin by CTA.
             int w = a.sched ? (int)atomicAdd(a.sched, 1u) : (int)blockIdx.x;
             for (;; ++it_local) {
-                // Publish (item, key tiles) in slot it & 1 for the MMA thread and the
-                // softmax warps; the slot's previous item (it - 2) has been read by all.
+                // Publish (item, key tiles | second tile present << 31) in slot it & 1 for
+                // the MMA warp and the softmax warps; the slot's previous item (it - 2)
+                // has been read by all.
                 const uint32_t sl = it_local & 1;
                 if (it_local >= 2 &&
                     !mbar_wait(bar(C::B_ITEMEMPTY + sl), ((it_local >> 1) - 1) & 1, abort, a.err, lim)) {
@@ -217,56 +353,62 @@ __global__ void __launch_bounds__(256, 1)
                     mbar_arrive(bar(C::B_ITEMFULL + sl));
                     break;
                 }
-                const QTile qt = work_item(g, w);
+                const QPair p = work_pair(g, w);
+                const bool has1 = p.q1.len > 0;
                 misc[4 + sl] = (uint32_t)w;
-                misc[2 + sl] = (uint32_t)kwalk_count(g, qt);
+                misc[2 + sl] = (uint32_t)pair_count(g, p) | (has1 ? 0x80000000u : 0u);
                 mbar_arrive(bar(C::B_ITEMFULL + sl));
                 if (it_local > 0 && !mbar_wait(bar(C::B_QEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
+                mbar_arrive_expect_tx(bar(C::B_QFULL), (has1 ? 2 : 1) * C::TILE_BYTES);
                 for (int bx = 0; bx < C::NBOX; ++bx)
-                    tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, qt.row0, qt.h, qt.b, bar(C::B_QFULL));
+                    tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, p.q0.row0, p.q0.h, p.q0.b, bar(C::B_QFULL));
+                if (has1)
+                    for (int bx = 0; bx < C::NBOX; ++bx)
+                        tma_load_4d(sQ + C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, p.q1.row0, p.q0.h, p.q0.b,
+                                    bar(C::B_QFULL));
                 ++qfills;
                 KWalk wk;
-                kwalk_begin(g, qt, wk);
+                kwalk_begin(g, p.span, wk);
                 KTile kt;
+                int c0, c1;
                 int prev_row = -1;   // k/v row of the tile whose V is still to be loaded
                 for (;;) {
-                    const bool more = kwalk_next(g, qt, wk, kt);
+                    const bool more = pair_next(g, p, wk, kt, c0, c1);
                     if (more) {
                         const uint32_t st = kfill % C::KS, use = kfill / C::KS;
-                        if (use > 0 && !mbar_wait(bar(C::B_SFULL + st), (use - 1) & 1, abort, a.err, lim)) {
+                        if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
-                        // Describe tile kfill for the softmax warps in slot kfill % TIR.  QK of
-                        // tile kfill - 3 has completed (the wait above), so the softmax has
-                        // finished tile kfill - 6 (QK(j) is issued after PV(j - 3)) and has
-                        // read every description older than that, including this slot's last.
+                        // Describe tile kfill in slot kfill % TIR.  Both products of tile
+                        // kfill - KS have completed (the wait above), and QK_x(j) is issued
+                        // after PV_x(j - 1): each group has read every description up to
+                        // kfill - KS - 1, including this slot's last (TIR > KS + 1).
                         {
                             const uint32_t e = (kfill % C::TIR) * 4;
                             tinfo[e] = (uint32_t)kt.pos0;
-                            tinfo[e + 1] = (uint32_t)kt.len | ((uint32_t)kt.cls << 16);
+                            tinfo[e + 1] = (uint32_t)kt.len | ((uint32_t)c0 << 16) | ((uint32_t)c1 << 20);
                             st_release_shared(sTI + e * 4 + 8, kfill + 1);
                         }
                         mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, qt.h,
-                                        qt.b, bar(C::B_KFULL + st));
+                            tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, p.q0.h,
+                                        p.q0.b, bar(C::B_KFULL + st));
                         ++kfill;
                     }
                     if (prev_row >= 0) {
                         const uint32_t st = vfill % C::VS, use = vfill / C::VS;
-                        if (use > 0 && !mbar_wait(bar(C::B_PVDONE + st), (use - 1) & 1, abort, a.err, lim)) {
+                        if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, prev_row, qt.h,
-                                        qt.b, bar(C::B_VFULL + st));
+                            tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, prev_row, p.q0.h,
+                                        p.q0.b, bar(C::B_VFULL + st));
                         ++vfill;
                     }
                     if (!more) break;
@@ -293,51 +435,55 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Per key tile j: QK(j) -> S[j % 3] once K(j) has landed, and PV(j - 2)
-        // once the softmax has written P(j - 2) and V(j - 2) has landed.  QK(j)
-        // overwrites the buffer that held P(j - 3), which PV(j - 3), issued just
-        // before, has read: the tensor pipe executes in issue order, so no
-        // separate "S free" barrier is needed.
-        // The whole warp runs this loop converged (waits, counters, descriptors);
-        // each MMA and commit is issued by one elected lane.
+        // Per item: QK_0(0), QK_1(0); then for each key tile j: PV_0(j) once group 0
+        // has written P_0(j), QK_0(j+1) into S_0 (over P_0(j), which PV_0(j), issued
+        // just before, has read: the tensor pipe executes in issue order), and the
+        // same for group 1.  The whole warp runs this loop converged (waits,
+        // counters, descriptors); each MMA and commit is issued by one elected lane.
         {
             uint32_t it_local = 0;
-            uint32_t qb = 0, qph = 0;   // buffer / stage index and phase of the next QK
-            uint32_t pb = 0, pph = 0;   // buffer / stage index and phase of the next PV
+            uint32_t kst = 0, kph = 0;   // K stage and phase of the next QK
+            uint32_t vst = 0, vph = 0;   // V stage and phase of the next PV
+            uint32_t pc[2] = {0, 0};     // PV_x issued so far (P_FULL[x] phases)
+            uint32_t oc[2] = {0, 0};     // items finished by group x (O_EMPTY[x] phases)
             bool ok = true;
             const uint64_t qdesc0 = sdesc(sQ, 16, 1024);            // K-major, 128B swizzle
             const uint64_t kdesc0 = sdesc(sK, 16, 1024);
             const uint64_t vdesc0 = sdesc(sV, C::BOX_BYTES, 1024);   // MN-major
             // descriptor start-address fields advance by bytes / 16
             constexpr uint32_t STAGE16 = C::TILE_BYTES >> 4;
-            auto qk = [&]() -> bool {
-                if (!warp_wait(bar(C::B_KFULL + qb), qph, abort, a.err, lim)) return false;
-                const uint64_t kd = kdesc0 + (uint64_t)(qb * STAGE16);
-                const uint32_t sd = tmem + C::S_COL + qb * 128;
+            auto qk = [&](int x) {
+                const uint64_t qd = qdesc0 + (uint64_t)(x * STAGE16);
+                const uint64_t kd = kdesc0 + (uint64_t)(kst * STAGE16);
+                const uint32_t sd = tmem + C::S_COL + x * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                    mma_ss_one(sd, qdesc0 + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    mma_ss_one(sd, qd + off, kd + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
                 }
-                mma_commit_one(bar(C::B_SFULL + qb));
-                qb = qb == C::NSB - 1 ? 0 : qb + 1;
-                qph ^= qb == 0;
-                return true;
+                mma_commit_one(bar(C::B_SFULL + x));
             };
-            auto pv = [&](bool first) -> bool {
-                if (!warp_wait(bar(C::B_PFULL + pb), pph, abort, a.err, lim)) return false;
-                if (!warp_wait(bar(C::B_VFULL + pb), pph, abort, a.err, lim)) return false;
+            auto pv = [&](int x, bool first) -> bool {
+                if (!warp_wait(bar(C::B_PFULL + x), pc[x] & 1, abort, a.err, lim)) return false;
+                ++pc[x];
                 tc_fence_after();   // P was written by the softmax warps' tcgen05.st
-                const uint64_t vd = vdesc0 + (uint64_t)(pb * STAGE16);
-                const uint32_t pa = tmem + C::S_COL + pb * 128;
+                const uint64_t vd = vdesc0 + (uint64_t)(vst * STAGE16);
+                const uint32_t pa = tmem + C::S_COL + x * 128;
 #pragma unroll
                 for (int kk = 0; kk < TILE / 16; ++kk)
-                    mma_ts_one(tmem + C::O_COL, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
+                    mma_ts_one(tmem + C::O_COL + x * D, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
                                (first && kk == 0) ? 0u : 1u);
-                mma_commit_one(bar(C::B_PVDONE + pb));
-                pb = pb == C::NSB - 1 ? 0 : pb + 1;
-                pph ^= pb == 0;
+                mma_commit_one(bar(C::B_PVDONE + x));
                 return true;
+            };
+            auto next_k = [&]() {
+                kst = kst == C::KS - 1 ? 0 : kst + 1;
+                kph ^= kst == 0;
+            };
+            // O_x of group x's previous item must have been read out before this
+            // item's first PV_x writes O_x (and before O_FULL[x]): waited once per item.
+            auto o_free = [&](int x) -> bool {
+                return oc[x] == 0 || warp_wait(bar(C::B_OEMPTY + x), (oc[x] - 1) & 1, abort, a.err, lim);
             };
             for (;; ++it_local) {
                 const uint32_t sl = it_local & 1;
@@ -345,34 +491,57 @@ __global__ void __launch_bounds__(256, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t item = misc[4 + sl], n = misc[2 + sl];
+                const uint32_t item = misc[4 + sl], nn = misc[2 + sl];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
                 if (item == 0xffffffffu) break;
+                const uint32_t n = nn & 0x7fffffffu;
+                const int ng = (nn >> 31) ? 2 : 1;   // query tiles in the pair
                 if (!warp_wait(bar(C::B_QFULL), it_local & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
-                // QK(0), QK(1); Q_EMPTY is committed right after the item's last QK.
-                if (n == 0) mma_commit_one(bar(C::B_QEMPTY));
-                if (n >= 1 && !(ok = qk())) break;
+                if (n == 0) {
+                    mma_commit_one(bar(C::B_QEMPTY));
+                    for (int x = 0; x < ng && ok; ++x) {
+                        if (!(ok = o_free(x))) break;
+                        mma_commit_one(bar(C::B_OFULL + x));
+                        ++oc[x];
+                    }
+                    if (!ok) break;
+                    continue;
+                }
+                // tile 0: both QKs, then the K stage and (one tile) Q are released
+                if (!(ok = warp_wait(bar(C::B_KFULL + kst), kph, abort, a.err, lim))) break;
+                for (int x = 0; x < ng; ++x) qk(x);
+                mma_commit_one(bar(C::B_KEMPTY + kst));
                 if (n == 1) mma_commit_one(bar(C::B_QEMPTY));
-                if (n >= 2 && !(ok = qk())) break;
-                if (n == 2) mma_commit_one(bar(C::B_QEMPTY));
-                // O of the previous item must have been read out before this item's
-                // first PV writes O (and before O_FULL): waited once per item, so
-                // the O_FULL / O_EMPTY phases never run two ahead of their waiters.
-                if (it_local > 0 && !(ok = warp_wait(bar(C::B_OEMPTY), (it_local - 1) & 1, abort, a.err, lim)))
-                    break;
-                for (uint32_t t = 2; t < n; ++t) {
-                    if (!(ok = qk())) break;
-                    if (t + 1 == n) mma_commit_one(bar(C::B_QEMPTY));
-                    if (!(ok = pv(t == 2))) break;
+                next_k();
+                for (uint32_t j = 0; j < n && ok; ++j) {
+                    const bool last = j + 1 == n;
+                    if (!(ok = warp_wait(bar(C::B_VFULL + vst), vph, abort, a.err, lim))) break;
+                    for (int x = 0; x < ng; ++x) {
+                        if (j == 0 && !(ok = o_free(x))) break;
+                        if (!(ok = pv(x, j == 0))) break;
+                        if (last) {
+                            mma_commit_one(bar(C::B_OFULL + x));
+                        } else {
+                            if (x == 0 && !(ok = warp_wait(bar(C::B_KFULL + kst), kph, abort, a.err, lim))) break;
+                            qk(x);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_one(bar(C::B_VEMPTY + vst));   // V(j) free once PV_0(j), PV_1(j) complete
+                    vst = vst == C::VS - 1 ? 0 : vst + 1;
+                    vph ^= vst == 0;
+                    if (!last) {
+                        mma_commit_one(bar(C::B_KEMPTY + kst));   // K(j+1) free once QK_0(j+1), QK_1(j+1) complete
+                        if (j + 2 == n) mma_commit_one(bar(C::B_QEMPTY));
+                        next_k();
+                    }
                 }
                 if (!ok) break;
-                if (n >= 2 && !(ok = pv(n == 2))) break;
-                if (n >= 1 && !(ok = pv(n == 1))) break;
-                mma_commit_one(bar(C::B_OFULL));
+                for (int x = 0; x < ng; ++x) ++oc[x];
             }
             if (!ok) {
                 // Wait for the MMAs already issued before TMEM is released.
@@ -382,35 +551,45 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax / epilogue
-        const int row = (warp & 3) * 32 + lane;
-        const uint32_t lane_addr = ((uint32_t)((warp & 3) * 32) << 16);
+        const int x = (warp - 2) >> 2;                 // group: query tile of the pair
+        const int quad = warp & 3;                     // TMEM lanes 32 quad .. + 31
+        const int row = quad * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const uint32_t scol = C::S_COL + (uint32_t)x * 128, ocol = C::O_COL + (uint32_t)x * D;
         const float sl2 = a.scale_log2;
-        uint32_t it_local = 0;
-        uint32_t sb = 0, sph = 0;   // S buffer and phase of the next tile
-        uint32_t pvb = 0, pvph = 0; // S buffer and phase of the previous tile (valid once n > 0)
-        uint32_t tcnt = 0;          // key tiles described so far (ring position)
+        uint32_t sx = 0;     // S_x completions seen (S_FULL[x] phases)
+        uint32_t tx = 0;     // P_x tiles stored (the previous one's PV_x is PV_DONE[x] phase tx - 1)
+        uint32_t ox = 0;     // items finished (O_FULL[x] phases)
+        uint32_t tcnt = 0;   // key tiles described so far (ring position)
         bool ok = true;
-        for (;; ++it_local) {
+        for (uint32_t it_local = 0;; ++it_local) {
             const uint32_t sl = it_local & 1;
             if (!warp_wait(bar(C::B_ITEMFULL + sl), (it_local >> 1) & 1, abort, a.err, lim)) {
                 ok = false;
                 break;
             }
-            const uint32_t item = misc[4 + sl], n_tiles = misc[2 + sl];
+            const uint32_t item = misc[4 + sl], nn = misc[2 + sl];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_ITEMEMPTY + sl));
             if (item == 0xffffffffu) break;
-            const QTile qt = work_item(g, (int)item);
+            const uint32_t n_tiles = nn & 0x7fffffffu;
+            if (x == 1 && !(nn >> 31)) {   // the pair holds one tile: nothing for group 1
+                tcnt += n_tiles;
+                continue;
+            }
+            const QPair pr = work_pair(g, (int)item);
+            const QTile qt = x ? pr.q1 : pr.q0;
             const long long qpos = qt.pos0 + row;
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;
             for (uint32_t j = 0; j < n_tiles; ++j) {
-                if (!warp_wait(bar(C::B_SFULL + sb), sph, abort, a.err, lim)) {
+                if (!warp_wait(bar(C::B_SFULL + x), sx & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
+                ++sx;
                 // The producer walked the tiles; take this one's position, length and
                 // class (written before K of the tile was loaded, so normally present).
                 KTile kt;
@@ -424,7 +603,7 @@ __global__ void __launch_bounds__(256, 1)
                     ++tcnt;
                     kt.pos0 = (long long)dx;
                     kt.len = (int)(dy & 0xffffu);
-                    kt.cls = (int)(dy >> 16);
+                    kt.cls = (int)((dy >> (16 + 4 * x)) & 15u);
                 }
                 tc_fence_after();
                 float s[TILE];
@@ -432,71 +611,70 @@ __global__ void __launch_bounds__(256, 1)
                     uint32_t r[TILE];
 #pragma unroll
                     for (int c = 0; c < TILE / 32; ++c)
-                        tmem_ld32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32,
-                                  *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+                        tmem_ld32(tmem + lane_addr + scol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < TILE; ++j) s[j] = __uint_as_float(r[j]);
+                    for (int j2 = 0; j2 < TILE; ++j2) s[j2] = __uint_as_float(r[j2]);
                 }
 
-                if (kt.cls == BA_TILE_PARTIAL || kt.len < TILE) {
+                // FULL tiles need no predicate; PARTIAL ones, and tiles EMPTY for this
+                // group's rows (seen only by the other tile of the pair), are masked.
+                if (kt.cls != BA_TILE_FULL || kt.len < TILE) {
                     const bool row_valid = row < qt.len;   // rows past the tile end are never stored
 #pragma unroll
-                    for (int c = 0; c < TILE / 32; ++c) mask_chunk(g, qt.b, qpos, row_valid, kt, c * 32, &s[c * 32]);
-                }
-                // p = 2^(s * scale * log2(e) - m) with m the running reference maximum,
-                // computed before this tile's maximum is known: the lazy rule keeps m
-                // unless the tile's maximum exceeds it by more than 2^8, so the tile
-                // maximum (ALU pipe) and the exponentials (MUFU / FMA pipes) run side by
-                // side, and only a row whose maximum did move redoes its exponentials.
-                // Arguments two lanes at a time, sums in four two-lane accumulators.
-                float sc[8];
-                uint32_t pk[TILE / 2];
-                auto exp_tile = [&](float m_use) {
+                    for (int c = 0; c < TILE / 32; ++c) {
+                        const uint32_t keep = keep_bits(g, qt.b, qpos, row_valid, kt.pos0, kt.len, c * 32);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) sc[k] = 0.f;
-#pragma unroll
-                    for (int j = 0; j < TILE / 2; ++j) {
-                        float x0, x1;
-                        ffma2_bc(s[2 * j], s[2 * j + 1], sl2, -m_use, x0, x1);
-                        const float p0 = fast_exp2(x0);
-                        const float p1 = fast_exp2(x1);
-                        fadd2_acc(sc[2 * (j & 3)], sc[2 * (j & 3) + 1], p0, p1);
-                        pk[j] = pack_bf16(p0, p1);
+                        for (int i = 0; i < 32; ++i)
+                            if (!((keep >> i) & 1u)) s[c * 32 + i] = -INFINITY;
                     }
-                };
-                exp_tile(m_ref == -INFINITY ? 0.f : m_ref);
-                // row maximum: 8 independent chains of three-input maxima, then a tree
+                }
+                // Row maximum first (8 independent chains of three-input maxima, then a
+                // tree).  The reference maximum m moves only when the tile's maximum
+                // exceeds it by more than 2^8 (lazy rule: the sums and O keep their scale
+                // otherwise; p stays below 2^8).
                 float mc[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mc[k] = fmaxf(s[k], s[8 + k]);
 #pragma unroll
-                for (int j = 16; j < TILE; j += 16) {
+                for (int j2 = 16; j2 < TILE; j2 += 16) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], s[j + k], s[j + 8 + k]);
+                    for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], s[j2 + k], s[j2 + 8 + k]);
                 }
                 const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), fmax3(fmax3(mc[3], mc[4], mc[5]), mc[6], mc[7]));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool resc = m_new > m_ref + 8.0f;   // true when m_ref = -inf and m_new finite
                 float alpha = 1.f;
-                if (__any_sync(0xffffffffu, resc)) {
-                    if (resc) {
-                        alpha = fast_exp2(m_ref - m_new);
-                        m_ref = m_new;
+                if (resc) {
+                    alpha = fast_exp2(m_ref - m_new);   // 0 when m_ref = -inf
+                    m_ref = m_new;
+                }
+                // p = 2^(s * scale * log2(e) - m), arguments two lanes at a time, sums in
+                // four two-lane accumulators; P (bf16) goes over the S columns already
+                // read, 16 columns (32 keys) at a time.
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                float sc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) sc[k] = 0.f;
+#pragma unroll
+                for (int c = 0; c < TILE / 32; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j2 = 0; j2 < 16; ++j2) {
+                        float x0, x1;
+                        ffma2_bc(s[32 * c + 2 * j2], s[32 * c + 2 * j2 + 1], sl2, -m_use, x0, x1);
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        fadd2_acc(sc[2 * (j2 & 3)], sc[2 * (j2 & 3) + 1], p0, p1);
+                        pk[j2] = pack_bf16(p0, p1);
                     }
-                    exp_tile(m_ref == -INFINITY ? 0.f : m_ref);   // rows that kept m repeat the same values
+                    tmem_st16(tmem + lane_addr + scol + c * 16, pk);
                 }
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;
-
-                // P over the first 64 columns of the S buffer just read
-#pragma unroll
-                for (int c = 0; c < TILE / 64; ++c)
-                    tmem_st32(tmem + lane_addr + C::S_COL + sb * 128 + c * 32,
-                              *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
                 if (__any_sync(0xffffffffu, resc) && n > 0) {
                     // O may be rescaled once PV of the previous tile has completed
-                    if (!warp_wait(bar(C::B_PVDONE + pvb), pvph, abort, a.err, lim)) {
+                    if (!warp_wait(bar(C::B_PVDONE + x), (tx - 1) & 1, abort, a.err, lim)) {
                         ok = false;
                         break;
                     }
@@ -504,28 +682,26 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(tmem + lane_addr + C::O_COL + c * 32, r);
+                        tmem_ld32(tmem + lane_addr + ocol + c * 32, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + lane_addr + C::O_COL + c * 32, r);
+                        tmem_st32(tmem + lane_addr + ocol + c * 32, r);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL + sb));
-                pvb = sb;
-                pvph = sph;
-                sb = sb == C::NSB - 1 ? 0 : sb + 1;
-                sph ^= sb == 0;
+                mbar_arrive(bar(C::B_PFULL + x));
+                ++tx;
                 ++n;
             }
             if (!ok) break;
             // epilogue
-            if (!warp_wait(bar(C::B_OFULL), it_local & 1, abort, a.err, lim)) {
+            if (!warp_wait(bar(C::B_OFULL + x), ox & 1, abort, a.err, lim)) {
                 ok = false;
                 break;
             }
+            ++ox;
             tc_fence_after();
             const bool valid = row < qt.len;
             const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + qt.row0 + row;
@@ -536,7 +712,7 @@ __global__ void __launch_bounds__(256, 1)
                 uint32_t r[32];
                 float o[32];
                 if (n > 0) {
-                    tmem_ld32(tmem + lane_addr + C::O_COL + c * 32, r);
+                    tmem_ld32(tmem + lane_addr + ocol + c * 32, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
@@ -548,7 +724,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             if (valid) a.lse[row_flat] = f.lse;
             tc_fence_before();
-            mbar_arrive(bar(C::B_OEMPTY));
+            mbar_arrive(bar(C::B_OEMPTY + x));
         }
     }
 
@@ -556,7 +732,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(C::TMEM_COLS)
                      : "memory");
     }
 }
@@ -569,7 +745,7 @@ int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return BA_ERR_CUDA;
     int grid = a.g.n_items < num_sms ? a.g.n_items : num_sms;
-    attn_tc_kernel<D><<<grid, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
+    attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -580,9 +756,12 @@ bool tc_supported(int dtype, int d) { return dtype == BA_BF16 && (d == 64 || d =
 size_t tc_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<64>::SMEM_BYTES; }
 
 int launch_attn_tc(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
-    if (a.g.n_items == 0) return BA_OK;
-    if (a.g.d == 128) return launch_d<128>(a, m, num_sms, s);
-    if (a.g.d == 64) return launch_d<64>(a, m, num_sms, s);
+    // The kernel's unit of work is a pair of query tiles (work_pair).
+    AttnArgs ap = a;
+    ap.g.n_items = n_pairs(a.g) * a.g.B * a.g.H;
+    if (ap.g.n_items == 0 || a.g.n_qtiles == 0) return BA_OK;
+    if (a.g.d == 128) return launch_d<128>(ap, m, num_sms, s);
+    if (a.g.d == 64) return launch_d<64>(ap, m, num_sms, s);
     return BA_ERR_SHAPE;
 }
 

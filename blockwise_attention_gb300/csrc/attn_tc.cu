@@ -169,15 +169,28 @@ __host__ __device__ inline int n_pairs(const Geom &g) {
     return (g.ring ? g.NC : 1) * pairs_per_chunk(g);
 }
 
-// Work item w -> pair.  Items are grouped by heads_per_group (b, h) pairs so
-// that concurrently running CTAs share K/V in L2; within a group the pairs
-// come heaviest first under causal masking (latest positions).
+// Work item w -> pair.  Pairs are dealt heaviest first under causal masking
+// (latest positions), in two phases.  Phase 1 holds every level but the
+// g.tail_levels lightest of each (b, h): grouped by heads_per_group (b, h) so
+// that concurrently running CTAs share K/V in L2.  Phase 2 deals the lightest
+// levels of all heads, heaviest first: the items claimed last are the smallest
+// of the launch, so the CTAs finish within about one small item of each other.
 __device__ inline QPair work_pair(const Geom &g, int w) {
     const int BH = g.B * g.H, G = g.heads_per_group, np = n_pairs(g);
-    const int per_group = G * np;
-    const int grp = w / per_group, rem = w % per_group;
-    const int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
-    const int pi = rem / g_heads, bh = grp * G + rem % g_heads;
+    const int tail = g.tail_levels < np ? g.tail_levels : np;
+    const int heavy = np - tail;
+    int pi, bh;
+    if (w < heavy * BH) {
+        const int per_group = G * heavy;
+        const int grp = w / per_group, rem = w % per_group;
+        const int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
+        pi = rem / g_heads;
+        bh = grp * G + rem % g_heads;
+    } else {
+        const int w2 = w - heavy * BH;
+        pi = heavy + w2 / BH;
+        bh = w2 % BH;
+    }
     const int pg = g.causal ? np - 1 - pi : pi;
     const int ppc = pairs_per_chunk(g), per = g.ring ? g.nqt_pc : g.n_qtiles;
     const int c = pg / ppc, i = pg % ppc;
@@ -758,7 +771,18 @@ size_t tc_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<64>::
 int launch_attn_tc(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
     // The kernel's unit of work is a pair of query tiles (work_pair).
     AttnArgs ap = a;
-    ap.g.n_items = n_pairs(a.g) * a.g.B * a.g.H;
+    const int np = n_pairs(a.g), BH = a.g.B * a.g.H;
+    ap.g.n_items = np * BH;
+    // Under causal masking, when each SM gets few items (fewer than 32), the
+    // lightest levels of every head go last, enough of them to give each SM about
+    // four small items at the end of the launch.  With many items per SM the
+    // heaviest-first order of each head group already ends on small items, and
+    // keeping the groups whole keeps their K/V in L2.
+    ap.g.tail_levels = 0;
+    if (a.g.causal && BH > 0 && (long long)np * BH < 32LL * num_sms) {
+        const int want = (4 * num_sms + BH - 1) / BH;
+        ap.g.tail_levels = want < np ? want : np;
+    }
     if (ap.g.n_items == 0 || a.g.n_qtiles == 0) return BA_OK;
     if (a.g.d == 128) return launch_d<128>(ap, m, num_sms, s);
     if (a.g.d == 64) return launch_d<64>(ap, m, num_sms, s);

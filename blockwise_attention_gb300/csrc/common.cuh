@@ -42,6 +42,7 @@ struct Geom {
     int nqt_pc, nkt_pc;      // tiles per q chunk / per k chunk
     int n_qtiles, n_ktiles;  // per (b, h)
     int heads_per_group;     // (b, h) pairs interleaved per group of work items
+    int tail_levels;         // lightest query-tile levels dealt last, across all heads (0: none)
     int n_items;             // n_qtiles * B * H
     int causal;
     const uint8_t *kpm;

@@ -598,13 +598,9 @@ __global__ void __launch_bounds__(320, 1)
             float m_ref = -INFINITY, l = 0.f;
             int n = 0;
             for (uint32_t j = 0; j < n_tiles; ++j) {
-                if (!warp_wait(bar(C::B_SFULL + x), sx & 1, abort, a.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                ++sx;
                 // The producer walked the tiles; take this one's position, length and
-                // class (written before K of the tile was loaded, so normally present).
+                // class (written before K of the tile was loaded, so normally present,
+                // and read before the scores arrive).
                 KTile kt;
                 {
                     const uint32_t e = (tcnt % C::TIR) * 4;
@@ -618,6 +614,11 @@ __global__ void __launch_bounds__(320, 1)
                     kt.len = (int)(dy & 0xffffu);
                     kt.cls = (int)((dy >> (16 + 4 * x)) & 15u);
                 }
+                if (!warp_wait(bar(C::B_SFULL + x), sx & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                ++sx;
                 tc_fence_after();
                 float s[TILE];
                 {

@@ -223,3 +223,32 @@ def test_rope_position_interpolation_bit_exact(dt, d, scale):
     # scale 1/4 at positions 4m reproduces plain RoPE at m
     m = torch.arange(T, dtype=torch.int32, device="cuda")
     assert torch.equal(ba.rope_apply(x, positions=4 * m, pos_scale=0.25), ba.rope_apply(x, positions=m))
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("ring", [False, True])
+def test_growing_scores_rescale(d, causal, ring):
+    """Scores that grow along the keys: the running maximum of a row moves by far
+    more than the kernel's lazy threshold (2^8 in exp2 units) several times after
+    the row's first key tile, so O and the sums are rescaled mid-row (the pages'
+    online softmax: every new maximum rescales the weighted sum already held)."""
+    B, H, T = 1, 2, 1024
+    g = torch.Generator(device="cpu").manual_seed(77)
+    q = torch.randn((B, H, T, d), generator=g) * 0.5
+    k = torch.randn((B, H, T, d), generator=g) * 0.5
+    v = torch.randn((B, H, T, d), generator=g)
+    # a common direction that later keys follow more and more: the scores of the
+    # last row run from about 0 to 14 (natural-log units) along the keys
+    q[..., 0] = 4.0
+    k[..., 0] = torch.linspace(0.0, 3.5 * math.sqrt(d), T).view(1, 1, T)
+    q, k, v = (x.to(torch.bfloat16).cuda() for x in (q, k, v))
+    if ring:
+        out, lse = ba.ring_attn_fwd(q, k, v, P=4, partition="zigzag", causal=causal, out_dtype=torch.float32)
+    else:
+        out, lse = ba.attn_block_fwd(q, k, v, causal=causal, out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=causal)
+    # the last row's maximum grows by more than twice the threshold across its tiles
+    s_last = (q.float()[0, 0, -1] @ k.float()[0, 0].T) / math.sqrt(d) * 1.4426950408889634
+    assert float(s_last[-128:].max() - s_last[:128].max()) > 2 * 8.0
+    compare(out, lse, o_ref, l_ref, "bf16", f"growing scores d={d} causal={causal} ring={ring}")

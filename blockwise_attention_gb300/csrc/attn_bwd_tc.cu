@@ -42,7 +42,9 @@ struct BCfg {
     static constexpr int VEC_OFF = 2 * TILE_BYTES;        // within a stage: 128 LSE (log2 units) + 128 D
     static constexpr int STG_BYTES = 2 * TILE_BYTES + 1024;
     static constexpr int BAR_OFF = STG_OFF + NST * STG_BYTES;
-    enum { B_RES = 0, B_FULL, B_EMPTY = B_FULL + NST, B_SFULL = B_EMPTY + NST, B_PFULL, B_DONE, B_DRAIN, NBAR };
+    // S_FULL[h], P_FULL[h]: half h (64 query / key columns) of the tile's scores and products
+    enum { B_RES = 0, B_FULL, B_EMPTY = B_FULL + NST, B_SFULL = B_EMPTY + NST, B_PFULL = B_SFULL + 2, B_DONE = B_PFULL + 2,
+           B_DRAIN, NBAR };
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort
     // At least 120 KB, so that one CTA occupies an SM: each CTA allocates all
     // 512 TMEM columns, and a second one would wait inside tcgen05.alloc.
@@ -51,8 +53,12 @@ struct BCfg {
     static constexpr uint32_t S_COL = 0, DP_COL = 128, ACC0_COL = 256, ACC1_COL = 256 + D;
     static constexpr uint32_t TMEM_COLS = 512;
     // kind::f16, fp32 accumulate, bf16 A and B, N >> 3 at 17, M >> 4 at 24
-    static constexpr uint32_t IDESC_SS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TILE >> 3) << 17) |
-                                         ((uint32_t)(TILE >> 4) << 24);
+    // Half a tile: 64 rows of the streamed operand (N of the score products, K of the
+    // gradient products), 8 KB into each 128B-swizzled box.
+    static constexpr int HALF = TILE / 2;
+    static constexpr int HALF_BYTES = HALF * 128;
+    static constexpr uint32_t IDESC_SS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(HALF >> 3) << 17) |
+                                         ((uint32_t)(TILE >> 4) << 24);   // M = 128, N = 64
     static constexpr uint32_t IDESC_TS = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          ((uint32_t)(D >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
 };
@@ -222,8 +228,10 @@ __device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_
             mbar_init(bar(C::B_FULL + i), full_count);
             mbar_init(bar(C::B_EMPTY + i), 1);
         }
-        mbar_init(bar(C::B_SFULL), 1);
-        mbar_init(bar(C::B_PFULL), 128);
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(bar(C::B_SFULL + hh), 1);
+            mbar_init(bar(C::B_PFULL + hh), 128);
+        }
         mbar_init(bar(C::B_DONE), 1);
         mbar_init(bar(C::B_DRAIN), 1);
         misc[1] = 0;
@@ -369,48 +377,75 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (converged)
+        // Each query tile is taken in two halves of 64 queries.  Per tile t:
+        // dV, dK += half 0 (once the elementwise warps stored its P^T, dS^T), then the
+        // next tile's half-0 scores, then dV, dK += half 1, then the next tile's
+        // half-1 scores: the scores of one half are computed while the elementwise
+        // warps work on the other.  Half h of S^T / dP^T lives in columns
+        // [64 h, 64 h + 64) of its region and its bf16 P^T / dS^T in the first 32 of
+        // them, so the next tile's half 0 never touches what half 1 still needs.
         bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
         const uint64_t kdesc = sdesc(sK, 16, 1024), vdesc = sdesc(sV, 16, 1024);   // K-major A operands
+        // S^T_h = K Q_h^T and dP^T_h = V dout_h^T (fp32 into TMEM) for the tile in stage st
+        auto scores = [&](int st, int hh) {
+            const uint32_t sQ = stage(st) + hh * C::HALF_BYTES, sDO = stage(st) + C::TILE_BYTES + hh * C::HALF_BYTES;
+            const uint64_t qk = sdesc(sQ, 16, 1024), dok = sdesc(sDO, 16, 1024);   // K-major B operands
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::S_COL + hh * C::HALF, kdesc + off, qk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::DP_COL + hh * C::HALF, vdesc + off, dok + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_one(bar(C::B_SFULL + hh));
+        };
+        // dV += P^T_h dout_h and dK += dS^T_h q_h for the tile in stage st
+        auto grads = [&](int st, int hh, uint32_t t, bool first) -> bool {
+            if (!warp_wait(bar(C::B_PFULL + hh), t & 1, abort, a.err, lim)) return false;
+            tc_fence_after();   // P^T and dS^T were written by the elementwise warps' tcgen05.st
+            const uint32_t sQ = stage(st), sDO = stage(st) + C::TILE_BYTES;
+            const uint64_t don = sdesc(sDO, C::BOX_BYTES, 1024), qn = sdesc(sQ, C::BOX_BYTES, 1024);   // MN-major B
+#pragma unroll
+            for (int kk = 0; kk < C::HALF / 16; ++kk)
+                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + hh * C::HALF + kk * 8,
+                           don + (uint64_t)((hh * C::HALF_BYTES + kk * 2048) >> 4), C::IDESC_TS,
+                           (first && kk == 0) ? 0u : 1u);   // dV += P^T dout
+#pragma unroll
+            for (int kk = 0; kk < C::HALF / 16; ++kk)
+                mma_ts_one(tmem + C::ACC1_COL, tmem + C::DP_COL + hh * C::HALF + kk * 8,
+                           qn + (uint64_t)((hh * C::HALF_BYTES + kk * 2048) >> 4), C::IDESC_TS,
+                           (first && kk == 0) ? 0u : 1u);   // dK += dS^T q
+            return true;
+        };
         uint32_t t = 0;
         PWalk pw;
         pwalk_begin(a, kt, true, pw);
         BTile pt;
-        while (ok && pwalk_next(a, kt, true, pw, pt)) {
-            const int st = t % C::NST;
-            if (!warp_wait(bar(C::B_FULL + st), (t / C::NST) & 1, abort, a.err, lim)) {
+        bool have = ok && pwalk_next(a, kt, true, pw, pt);
+        if (have) {
+            if (!warp_wait(bar(C::B_FULL), 0, abort, a.err, lim)) {
                 ok = false;
-                break;
+            } else {
+                scores(0, 0);
+                scores(0, 1);
             }
-            const uint32_t sQ = stage(st), sDO = stage(st) + C::TILE_BYTES;
-            const uint64_t qk = sdesc(sQ, 16, 1024), dok = sdesc(sDO, 16, 1024);   // K-major B operands
-            // S^T = K Q^T and dP^T = V dout^T (fp32 into TMEM)
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                mma_ss_one(tmem + C::S_COL, kdesc + off, qk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+        while (ok && have) {
+            const int st = t % C::NST, stn = (t + 1) % C::NST;
+            const bool more = pwalk_next(a, kt, true, pw, pt);
+            if (!(ok = grads(st, 0, t, t == 0))) break;
+            if (more) {
+                if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
+                scores(stn, 0);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                mma_ss_one(tmem + C::DP_COL, vdesc + off, dok + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_one(bar(C::B_SFULL));
-            if (!warp_wait(bar(C::B_PFULL), t & 1, abort, a.err, lim)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();   // P^T and dS^T were written by the elementwise warps' tcgen05.st
-            const uint64_t don = sdesc(sDO, C::BOX_BYTES, 1024), qn = sdesc(sQ, C::BOX_BYTES, 1024);   // MN-major B
-#pragma unroll
-            for (int kk = 0; kk < TILE / 16; ++kk)
-                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + kk * 8, don + (uint64_t)((kk * 2048) >> 4),
-                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dV += P^T dout
-#pragma unroll
-            for (int kk = 0; kk < TILE / 16; ++kk)
-                mma_ts_one(tmem + C::ACC1_COL, tmem + C::DP_COL + kk * 8, qn + (uint64_t)((kk * 2048) >> 4),
-                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dK += dS^T q
+            if (!(ok = grads(st, 1, t, false))) break;
             mma_commit_one(bar(C::B_EMPTY + st));
+            if (more) scores(stn, 1);
             ++t;
+            have = more;
         }
         if (ok) {
             mma_commit_one(bar(C::B_DONE));
@@ -434,16 +469,19 @@ __global__ void __launch_bounds__(256, 1)
         BTile pt;
         while (ok && pwalk_next(a, kt, true, pw, pt)) {
             const int st = t % C::NST;
-            if (!warp_wait(bar(C::B_SFULL), t & 1, abort, a.err, lim)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
             const uint32_t s_nlse = smem_u32(vec(st)), s_dd = s_nlse + TILE * 4;   // -LSE log2 units, D
             const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
 #pragma unroll
             for (int c = 0; c < TILE / 32; ++c) {
+                const int hh = c >> 1;   // half of the tile: queries [64 hh, 64 hh + 64)
+                if ((c & 1) == 0) {
+                    if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
                 uint32_t rs[32], rd[32];
                 tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
                 tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
@@ -471,13 +509,18 @@ __global__ void __launch_bounds__(256, 1)
                     pd[q4 * 2] = pack_bf16(dv[0], dv[1]);
                     pd[q4 * 2 + 1] = pack_bf16(dv[2], dv[3]);
                 }
-                // P^T / dS^T of these 32 queries into 16 columns the earlier chunks have read
-                tmem_st16(tmem + lane_addr + C::S_COL + c * 16, pp);
-                tmem_st16(tmem + lane_addr + C::DP_COL + c * 16, pd);
+                // P^T / dS^T of these 32 queries into 16 columns of this half that the
+                // earlier chunk of the half has read
+                const uint32_t pcol = hh * C::HALF + (c & 1) * 16;
+                tmem_st16(tmem + lane_addr + C::S_COL + pcol, pp);
+                tmem_st16(tmem + lane_addr + C::DP_COL + pcol, pd);
+                if (c & 1) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_PFULL + hh));
+                }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            if (!ok) break;
             ++t;
         }
         if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {
@@ -563,44 +606,66 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (converged)
+        // Each key tile is taken in two halves of 64 keys, in the order of the dK/dV
+        // kernel: dQ += half 0, the next tile's half-0 scores, dQ += half 1, the next
+        // tile's half-1 scores.  Half h of S / dP lives in columns [64 h, 64 h + 64)
+        // of its region and its bf16 dS in the first 32 of them.
         bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
         const uint64_t qdesc = sdesc(sQ, 16, 1024), dodesc = sdesc(sDO, 16, 1024);   // K-major A operands
+        // S_h = Q K_h^T and dP_h = dout V_h^T for the tile in stage st
+        auto scores = [&](int st, int hh) {
+            const uint32_t sK = stage(st) + hh * C::HALF_BYTES, sV = stage(st) + C::TILE_BYTES + hh * C::HALF_BYTES;
+            const uint64_t kk_ = sdesc(sK, 16, 1024), vk = sdesc(sV, 16, 1024);   // K-major B operands
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::S_COL + hh * C::HALF, qdesc + off, kk_ + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_one(tmem + C::DP_COL + hh * C::HALF, dodesc + off, vk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_one(bar(C::B_SFULL + hh));
+        };
+        // dQ += dS_h K_h for the tile in stage st
+        auto grads = [&](int st, int hh, uint32_t t, bool first) -> bool {
+            if (!warp_wait(bar(C::B_PFULL + hh), t & 1, abort, a.err, lim)) return false;
+            tc_fence_after();   // dS was written by the elementwise warps' tcgen05.st
+            const uint64_t kn = sdesc(stage(st), C::BOX_BYTES, 1024);   // K as the MN-major B operand
+#pragma unroll
+            for (int kk = 0; kk < C::HALF / 16; ++kk)
+                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + hh * C::HALF + kk * 8,
+                           kn + (uint64_t)((hh * C::HALF_BYTES + kk * 2048) >> 4), C::IDESC_TS,
+                           (first && kk == 0) ? 0u : 1u);   // dQ += dS K
+            return true;
+        };
         uint32_t t = 0;
         PWalk pw;
         pwalk_begin(a, qt, false, pw);
         BTile pt;
-        while (ok && pwalk_next(a, qt, false, pw, pt)) {
-            const int st = t % C::NST;
-            if (!warp_wait(bar(C::B_FULL + st), (t / C::NST) & 1, abort, a.err, lim)) {
+        bool have = ok && pwalk_next(a, qt, false, pw, pt);
+        if (have) {
+            if (!warp_wait(bar(C::B_FULL), 0, abort, a.err, lim)) {
                 ok = false;
-                break;
+            } else {
+                scores(0, 0);
+                scores(0, 1);
             }
-            const uint32_t sK = stage(st), sV = stage(st) + C::TILE_BYTES;
-            const uint64_t kk_ = sdesc(sK, 16, 1024), vk = sdesc(sV, 16, 1024);   // K-major B operands
-            // S = Q K^T and dP = dout V^T
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                mma_ss_one(tmem + C::S_COL, qdesc + off, kk_ + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
+        }
+        while (ok && have) {
+            const int st = t % C::NST, stn = (t + 1) % C::NST;
+            const bool more = pwalk_next(a, qt, false, pw, pt);
+            if (!(ok = grads(st, 0, t, t == 0))) break;
+            if (more) {
+                if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
+                scores(stn, 0);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                mma_ss_one(tmem + C::DP_COL, dodesc + off, vk + off, C::IDESC_SS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_one(bar(C::B_SFULL));
-            if (!warp_wait(bar(C::B_PFULL), t & 1, abort, a.err, lim)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();   // dS was written by the elementwise warps' tcgen05.st
-            const uint64_t kn = sdesc(sK, C::BOX_BYTES, 1024);   // K as the MN-major B operand
-#pragma unroll
-            for (int kk = 0; kk < TILE / 16; ++kk)
-                mma_ts_one(tmem + C::ACC0_COL, tmem + C::S_COL + kk * 8, kn + (uint64_t)((kk * 2048) >> 4),
-                           C::IDESC_TS, (t > 0 || kk > 0) ? 1u : 0u);   // dQ += dS K
+            if (!(ok = grads(st, 1, t, false))) break;
             mma_commit_one(bar(C::B_EMPTY + st));
+            if (more) scores(stn, 1);
             ++t;
+            have = more;
         }
         if (ok) {
             mma_commit_one(bar(C::B_DONE));
@@ -630,15 +695,18 @@ __global__ void __launch_bounds__(256, 1)
         pwalk_begin(a, qt, false, pw);
         BTile pt;
         while (ok && pwalk_next(a, qt, false, pw, pt)) {
-            if (!warp_wait(bar(C::B_SFULL), t & 1, abort, a.err, lim)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
             const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
 #pragma unroll
             for (int c = 0; c < TILE / 32; ++c) {
+                const int hh = c >> 1;   // half of the tile: keys [64 hh, 64 hh + 64)
+                if ((c & 1) == 0) {
+                    if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
                 uint32_t rs[32], rd[32];
                 tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
                 tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
@@ -658,12 +726,16 @@ __global__ void __launch_bounds__(256, 1)
                     }
                     pd[k2] = pack_bf16(dv[0], dv[1]);
                 }
-                // dS of these 32 keys into 16 columns the earlier chunks have read
-                tmem_st16(tmem + lane_addr + C::S_COL + c * 16, pd);
+                // dS of these 32 keys into 16 columns of this half that the earlier
+                // chunk of the half has read
+                tmem_st16(tmem + lane_addr + C::S_COL + hh * C::HALF + (c & 1) * 16, pd);
+                if (c & 1) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(C::B_PFULL + hh));
+                }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(C::B_PFULL));
+            if (!ok) break;
             ++t;
         }
         if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {

@@ -179,8 +179,12 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v,
  *  q_off, k_off, masks, causal, scale: as for attn_block_fwd.
  *  dq: (B, H, Lq, d), dk, dv: (B, H, Lk, d), fp32 contiguous, caller-owned.
  *  accumulate: 0 = overwrite dq, dk, dv; 1 = add this block's gradients.
- *  workspace: attn_block_bwd_workspace_size() bytes (the D_i vector).
- * Runs on the CUDA cores in fp32 (no tensor-core backward yet).
+ *  workspace: attn_block_bwd_workspace_size() bytes, 256-byte aligned, owned by
+ *    the caller (or NULL: allocated and freed on the stream): the D_i vector
+ *    (fp32 per row).
+ * bf16 with d = 64 or 128, TMA-legal strides and 16-byte aligned dq / dk / dv
+ * run on the tensor cores (tcgen05; P and dS rounded to bf16 for the
+ * products, fp32 accumulation); everything else runs on the CUDA cores in fp32.
  * Errors: BA_ERR_ARG (NULL pointers for non-empty sides, negative sizes or
  * offsets, masks not covering the global positions), BA_ERR_SHAPE (d not in
  * {16, 32, 64, 128}).

@@ -472,7 +472,9 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t s_nlse = smem_u32(vec(st)), s_dd = s_nlse + TILE * 4;   // -LSE log2 units, D
             const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
-#pragma unroll
+            // Not unrolled: four copies of this body did not fit the instruction cache
+            // (ncu: warps stalled mostly on instruction fetch).
+#pragma unroll 1
             for (int c = 0; c < TILE / 32; ++c) {
                 const int hh = c >> 1;   // half of the tile: queries [64 hh, 64 hh + 64)
                 if ((c & 1) == 0) {
@@ -697,7 +699,8 @@ __global__ void __launch_bounds__(256, 1)
         while (ok && pwalk_next(a, qt, false, pw, pt)) {
             const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                               (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
-#pragma unroll
+            // Not unrolled, as in the dK/dV kernel (instruction cache).
+#pragma unroll 1
             for (int c = 0; c < TILE / 32; ++c) {
                 const int hh = c >> 1;   // half of the tile: keys [64 hh, 64 hh + 64)
                 if ((c & 1) == 0) {

@@ -98,7 +98,7 @@ EXPORTED = ["attn_block_fwd", "attn_block_fwd_workspace_size", "attn_merge", "ri
             "ba_sync_status", "ba_debug_wait_timeout", "ba_strerror", "attn_block_fwd_noalloc",
             "attn_block_bwd", "attn_block_bwd_workspace_size", "ring_attn_bwd", "ring_attn_bwd_workspace_size",
             "ulysses_all_to_all", "ulysses_attn_fwd", "ulysses_attn_fwd_workspace_size",
-            "attn_decode_fwd", "attn_decode_workspace_size"]
+            "attn_decode_fwd", "attn_decode_workspace_size", "ba_pair_schedule"]
 
 
 def load(path: str | None = None):
@@ -134,6 +134,8 @@ def load(path: str | None = None):
     lib.ba_tile_classes.argtypes = [i, i, i, i64, i64, vp, i64, vp, i64, i, vp, vp]
     lib.ba_index_maps.restype = i
     lib.ba_index_maps.argtypes = [i, i, i, vp, vp]
+    lib.ba_pair_schedule.restype = i
+    lib.ba_pair_schedule.argtypes = [i, i, i, i, i, i, i, vp, ctypes.c_int64]
     lib.ba_sync_status.restype = i
     lib.ba_sync_status.argtypes = [vp]
     lib.ba_debug_wait_timeout.restype = i
@@ -519,6 +521,21 @@ def index_maps(T, P, partition="contiguous"):
     _check("ba_index_maps", lib.ba_index_maps(T, P, PARTITIONS[partition], tok.ctypes.data_as(ctypes.c_void_p),
                                               sch.ctypes.data_as(ctypes.c_void_p)))
     return tok.reshape(P, T // P), sch.reshape(P, P)
+
+
+def pair_schedule(B, H, T, P, partition="zigzag", causal=True, num_sms=152):
+    """Host, exact: the tensor-core forward kernel's work items for a ring_attn_fwd
+    launch without masks, in dealing order, as an (n, 8) int32 array of
+    (b, h, tile-0 row0, tile-0 rows, tile-1 row0, tile-1 rows, key tiles, phase)."""
+    import numpy as np
+    lib = load()
+    n = lib.ba_pair_schedule(B, H, T, P, PARTITIONS[partition], int(causal), num_sms, None, 0)
+    _check("ba_pair_schedule", min(n, 0))
+    items = np.zeros((max(n, 0), 8), dtype=np.int32)
+    if n > 0:
+        _check("ba_pair_schedule", min(lib.ba_pair_schedule(B, H, T, P, PARTITIONS[partition], int(causal), num_sms,
+                                                            items.ctypes.data_as(ctypes.c_void_p), n), 0))
+    return items
 
 
 def sync_status(stream=None) -> int:

@@ -530,6 +530,51 @@ const char *ba_strerror(int code) {
     }
 }
 
+int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int num_sms, int32_t *items,
+                     int64_t capacity) {
+    if (B < 0 || H < 0 || T < 0 || P < 1 || num_sms < 1 || capacity < 0) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
+    if (T % NC) return BA_ERR_SHAPE;
+    if ((long long)B * H == 0 || T == 0) return 0;
+    // the geometry ring_attn_fwd builds for a fused launch without masks (d = 128, bf16)
+    Geom g;
+    std::memset(&g, 0, sizeof g);
+    g.B = B;
+    g.H = H;
+    g.d = 128;
+    g.ring = 1;
+    g.T = T;
+    g.P = P;
+    g.zigzag = partition == BA_PART_ZIGZAG;
+    g.NC = NC;
+    g.CL = T / NC;
+    g.nqt_pc = g.nkt_pc = ceil_div(g.CL, TILE);
+    g.n_qtiles = g.n_ktiles = NC * g.nqt_pc;
+    g.heads_per_group = heads_per_group(B, H, T, 128, BA_BF16);
+    g.causal = causal != 0;
+    g.s_begin = 0;
+    g.s_end = P;
+    const long long n = (long long)n_pairs(g) * B * H;
+    if (n > 0x7fffffffLL) return BA_ERR_SHAPE;
+    g.n_items = (int)n;
+    g.tail_levels = pair_tail_levels(g, num_sms);
+    const int heavy_items = (n_pairs(g) - g.tail_levels) * B * H;
+    for (long long w = 0; items && w < n && w < capacity; ++w) {
+        const QPair p = work_pair(g, (int)w);
+        int32_t *o = items + 8 * w;
+        o[0] = p.q0.b;
+        o[1] = p.q0.h;
+        o[2] = p.q0.row0;
+        o[3] = p.q0.len;
+        o[4] = p.q1.row0;
+        o[5] = p.q1.len;
+        o[6] = pair_count(g, p);
+        o[7] = w < heavy_items ? 0 : 1;
+    }
+    return (int)n;
+}
+
 int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule) {
     if (T < 0 || P < 1) return BA_ERR_ARG;
     if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG && partition != BA_PART_STRIPED)

@@ -288,6 +288,141 @@ __device__ inline bool excluded(const Geom &g, int b, long long qp, long long kp
 }
 
 // ---------------------------------------------------------------------------
+// Pairs of query tiles (the tensor-core kernel's unit of work)
+// ----------------------------------------------------------------------------
+//
+// The unit of work is a pair of adjacent query tiles of one chunk (ring mode)
+// or of the block: tiles 2i and 2i + 1 of the chunk; when the chunk has an odd
+// number of tiles its last pair holds one tile.  The two tiles cover
+// consecutive positions, so the pair's key walk is the walk of the 256-row span
+// that covers both; each key tile of it carries one class per tile (a tile that
+// only the second query tile sees is EMPTY for the first, whose rows then see
+// no key in it).
+
+struct QPair {
+    QTile q0, q1;    // q1.len == 0 when the pair holds one tile
+    QTile span;      // both tiles as one query range (walk geometry)
+};
+
+__host__ __device__ inline int pairs_per_chunk(const Geom &g) {
+    const int per = g.ring ? g.nqt_pc : g.n_qtiles;
+    return (per + 1) / 2;
+}
+
+// Pairs per (b, h).
+__host__ __device__ inline int n_pairs(const Geom &g) {
+    return (g.ring ? g.NC : 1) * pairs_per_chunk(g);
+}
+
+// Work item w -> pair.  Pairs are dealt heaviest first under causal masking
+// (latest positions), in two phases.  Phase 1 holds every level but the
+// g.tail_levels lightest of each (b, h): grouped by heads_per_group (b, h) so
+// that concurrently running CTAs share K/V in L2.  Phase 2 deals the lightest
+// levels of all heads, heaviest first: the items claimed last are the smallest
+// of the launch, so the CTAs finish within about one small item of each other.
+__host__ __device__ inline QPair work_pair(const Geom &g, int w) {
+    const int BH = g.B * g.H, G = g.heads_per_group, np = n_pairs(g);
+    const int tail = g.tail_levels < np ? g.tail_levels : np;
+    const int heavy = np - tail;
+    int pi, bh;
+    if (w < heavy * BH) {
+        const int per_group = G * heavy;
+        const int grp = w / per_group, rem = w % per_group;
+        const int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
+        pi = rem / g_heads;
+        bh = grp * G + rem % g_heads;
+    } else {
+        const int w2 = w - heavy * BH;
+        pi = heavy + w2 / BH;
+        bh = w2 % BH;
+    }
+    const int pg = g.causal ? np - 1 - pi : pi;
+    const int ppc = pairs_per_chunk(g), per = g.ring ? g.nqt_pc : g.n_qtiles;
+    const int c = pg / ppc, i = pg % ppc;
+    const int b = bh / g.H, h = bh % g.H;
+    QPair p;
+    p.q0 = q_tile(g, c * per + 2 * i, b, h);
+    if (2 * i + 1 < per) {
+        p.q1 = q_tile(g, c * per + 2 * i + 1, b, h);
+    } else {
+        p.q1 = p.q0;
+        p.q1.len = 0;
+    }
+    p.span = p.q0;
+    p.span.len = p.q0.len + p.q1.len;
+    return p;
+}
+
+// Next key tile of the pair's walk that one of its query tiles sees, with the
+// class for each (c1 = EMPTY when the pair holds one tile); false at the end.
+__host__ __device__ __forceinline__ bool pair_next(const Geom &g, const QPair &p, KWalk &w, KTile &k, int &c0, int &c1) {
+    const int q0_last = (int)p.q0.pos0 + p.q0.len - 1;
+    const bool has1 = p.q1.len > 0;
+    for (;;) {
+        if (w.row >= w.chunk_end) {
+            if (!kwalk_next_chunk(g, w)) return false;
+            continue;
+        }
+        const int row = w.row;
+        const int pos = row + w.pos_off;
+        const int rem = w.chunk_end - row;
+        k.row0 = row;
+        k.len = rem < TILE ? rem : TILE;
+        k.pos0 = pos;
+        k.idx = w.idx;
+        w.row = row + TILE;
+        ++w.idx;
+        if (g.cls) {
+            const int8_t *m = g.cls + ((long long)p.q0.b * g.n_qtiles + p.q0.g) * g.n_ktiles + k.idx;
+            c0 = m[0];
+            c1 = has1 ? m[g.n_ktiles] : BA_TILE_EMPTY;
+            if (c0 == BA_TILE_EMPTY && c1 == BA_TILE_EMPTY) continue;
+            return true;
+        }
+        if (g.causal) {
+            if (pos > w.q_last) {          // this and the rest of the chunk lie in the future of both
+                w.row = w.chunk_end;
+                continue;
+            }
+            const int k_last = pos + k.len - 1;
+            c0 = pos > q0_last ? BA_TILE_EMPTY : (k_last <= (int)p.q0.pos0 ? BA_TILE_FULL : BA_TILE_PARTIAL);
+            c1 = !has1 ? BA_TILE_EMPTY : (k_last <= (int)p.q1.pos0 ? BA_TILE_FULL : BA_TILE_PARTIAL);
+        } else {
+            c0 = BA_TILE_FULL;
+            c1 = has1 ? BA_TILE_FULL : BA_TILE_EMPTY;
+        }
+        if (g.kpm || g.am) {   // masks need predicates
+            if (c0 == BA_TILE_FULL) c0 = BA_TILE_PARTIAL;
+            if (c1 == BA_TILE_FULL) c1 = BA_TILE_PARTIAL;
+        }
+        return true;
+    }
+}
+
+// Number of key tiles pair_next yields for pair p.
+__host__ __device__ inline int pair_count(const Geom &g, const QPair &p) {
+    if (!g.cls) return kwalk_count(g, p.span);   // the span's walk: both tiles see a tile the span sees
+    KWalk w;
+    kwalk_begin(g, p.span, w);
+    KTile k;
+    int c0, c1, n = 0;
+    while (pair_next(g, p, w, k, c0, c1)) ++n;
+    return n;
+}
+
+// Lightest levels dealt last (work_pair's phase 2) for a launch on num_sms SMs:
+// under causal masking, when each SM gets fewer than 32 items, enough of them to
+// give each SM about four small items at the end of the launch.  With many items
+// per SM the heaviest-first order of each head group already ends on small items,
+// and keeping the groups whole keeps their K/V in L2.
+__host__ __device__ inline int pair_tail_levels(const Geom &g, int num_sms) {
+    const int np = n_pairs(g), BH = g.B * g.H;
+    if (!g.causal || BH <= 0 || (long long)np * BH >= 32LL * num_sms) return 0;
+    const int want = (4 * num_sms + BH - 1) / BH;
+    return want < np ? want : np;
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier helpers with bounded waits
 // ---------------------------------------------------------------------------
 

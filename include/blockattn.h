@@ -337,6 +337,23 @@ int ba_tile_classes(int B, int Lq, int Lk, int64_t q_off, int64_t k_off,
 int ba_index_maps(int T, int P, int partition, int32_t *tok_of, int32_t *schedule);
 
 /*
+ * ba_pair_schedule -- host, exact integers: the work items of the tensor-core
+ * forward kernel for a ring_attn_fwd launch without masks (causal or not) over
+ * B x H heads of T tokens, P ranks, on num_sms SMs, in the order the kernel
+ * deals them.  An item is a pair of adjacent 128-row query tiles of one chunk
+ * (a chunk with an odd tile count ends in a one-tile pair) with the key tiles
+ * its walk visits.  items (nullable): capacity rows of 8 int32, item w at
+ * items[8 w ..]: b, h, first query row of tile 0, its rows, first query row of
+ * tile 1, its rows (0: no second tile), key tiles visited, phase (0: grouped
+ * by heads, heaviest first; 1: the lightest levels of all heads, dealt last).
+ * Returns the number of items (every item is written when capacity allows),
+ * or BA_ERR_SHAPE for indivisible T, BA_ERR_ARG for bad sizes.  Computed by
+ * the same functions the kernel uses; for tests and inspection.
+ */
+int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int num_sms,
+                     int32_t *items, int64_t capacity);
+
+/*
  * attn_block_fwd_noalloc -- attn_block_fwd for callers that cannot allocate
  * device memory.  The pages have no counterpart; this is a library-level
  * variant.  Some hosts own every device allocation themselves (for example a

@@ -116,22 +116,6 @@ __host__ __device__ inline KTile k_tile_by_id(const Geom &g, int kg) {
     return t;
 }
 
-// Number of positions in the key-tile walk of one query tile (EMPTY tiles
-// included; they are skipped by the caller).
-__host__ __device__ inline int walk_length(const Geom &g) {
-    if (!g.ring) return g.n_ktiles;
-    return (g.s_end - g.s_begin) * (g.zigzag ? 2 : 1) * g.nkt_pc;
-}
-
-// Causal class of (q tile, k tile) from positions alone.
-__host__ __device__ inline int causal_class(const QTile &q, const KTile &k) {
-    long long q_last = q.pos0 + q.len - 1;
-    long long k_last = k.pos0 + k.len - 1;
-    if (k.pos0 > q_last) return BA_TILE_EMPTY;
-    if (k_last <= q.pos0) return BA_TILE_FULL;
-    return BA_TILE_PARTIAL;
-}
-
 // Incremental walk over the key tiles a query tile visits, in ring order,
 // with EMPTY tiles skipped.  Every role of a kernel runs the same walk, so they
 // agree on the sequence without communicating.  Without a class map, causal

@@ -47,7 +47,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses", "decode"],
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="time the oracle over the whole workload instead of a sample (small workloads)")
+    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses", "decode", "merge"],
                     help="ulysses: time ulysses_attn_fwd over P head-partitioned ranks (not the default line)")
     ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
                     help="backward: time ring_attn_bwd instead (not the default bench line)")
@@ -100,6 +102,30 @@ def profiled_traffic(workload: str):
         with open(os.path.join(ROOT, src), "rb") as f:
             sha.update(f.read())
     return int(t.group(1)) if sha.hexdigest() == h.group(1) else None
+
+
+# Dense bf16 tensor throughput of one SM per clock: one 128 x 128 x 16 MMA
+# (kind::f16, cta_group::1) every 64 cycles, as measured on this part.
+TENSOR_FLOP_PER_CLK_SM = 2 * 128 * 128 * 16 // 64
+NUM_SMS = 152
+
+
+def tensor_roofline(achieved, peaks, peak_src, clocks, timed_s):
+    """Roofline object of a tensor-bound kernel.  It is graded against the
+    measured burst bf16 peak (a cuBLAS GEMM timed best-of-10): the timed region
+    lasts well under a second, while the measured sustained peak describes a
+    GEMM looped for seconds under the power cap at a lower clock.  The
+    clock-derived tensor peak at the sampled SM clock is given beside it."""
+    burst = float(peaks["bf16_tflops"])
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    at_clock = TENSOR_FLOP_PER_CLK_SM * NUM_SMS * mhz * 1e6 / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
+            "peak_source": f"{peak_src} bf16_tflops (burst; the timed region lasts {timed_s:.2f} s)",
+            "frac_of_sustained_peak": achieved / sustained,
+            "tensor_peak_at_clock": at_clock, "frac_of_peak_at_clock": achieved / at_clock,
+            "peak_at_clock_source": f"{TENSOR_FLOP_PER_CLK_SM} FLOP/clk/SM x {NUM_SMS} SMs x median SM clock "
+                                    f"{mhz:.0f} MHz"}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -171,10 +197,11 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
-def oracle_cpu_baseline(w, inp_cpu_head, seconds):
+def oracle_cpu_baseline(w, inp_cpu_head, seconds, kpm=None, am=None):
     """Time the oracle, as it stands, on sampled query rows of one head (each
-    row over its full causal key range), RoPE included.  Returns the JSON
-    object for `cpu_baseline`."""
+    row over its full key range, with the workload's exclusions), RoPE
+    included.  kpm: (1, T) key-padding row of that head's batch item; am:
+    (T, T).  Returns the JSON object for `cpu_baseline`."""
     import oracle
     q, k, v = inp_cpu_head            # (1, 1, T, d) float32 tensors on the CPU
     T, d = w.T, w.d
@@ -187,9 +214,21 @@ def oracle_cpu_baseline(w, inp_cpu_head, seconds):
         return (oracle.rope(q, base=w.rope_base, round_to=w.dtype),
                 oracle.rope(k, base=w.rope_base, round_to=w.dtype))
 
+    vis = None
+    if kpm is not None or am is not None:
+        vis = np.ones((T, T), dtype=bool)
+        if w.causal:
+            vis &= np.tri(T, dtype=bool)
+        if kpm is not None:
+            vis &= (np.asarray(kpm).reshape(-1)[:T] == 0)[None, :]
+        if am is not None:
+            vis &= np.asarray(am) == 0
+
     def attend(qr, kr, nrows):
         rows = np.sort(rng.choice(T, size=nrows, replace=False)).astype(np.int64)
-        oracle.attention(qr, kr, v, causal=w.causal, rows=rows, nthreads=threads)
+        oracle.attention(qr, kr, v, causal=w.causal, kpm=kpm, am=am, rows=rows, nthreads=threads)
+        if vis is not None:
+            return int(vis[rows].sum())
         return int((rows + 1).sum()) if w.causal else nrows * T
 
     # calibrate: RoPE of the head is a fixed cost, attention scales with the rows
@@ -209,8 +248,28 @@ def oracle_cpu_baseline(w, inp_cpu_head, seconds):
     flops = 4.0 * d * pairs
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} random query rows of one head (b=0, h=0) of {w.name}, each over its full "
-                      f"causal key range, RoPE of that head's Q and K included; {pairs} visible pairs "
-                      f"in {dt:.2f} s"}
+                      f"key range with the workload's exclusions, RoPE of that head's Q and K included "
+                      f"when the workload rotates; {pairs} visible pairs in {dt:.2f} s"}
+
+
+def oracle_full_baseline(w, inp):
+    """Time the oracle, as it stands, over the whole workload (every row of
+    every head, RoPE included) on the host's cores."""
+    import oracle
+    threads = oracle.default_threads()
+    q, k, v = inp.q.float().cpu(), inp.k.float().cpu(), inp.v.float().cpu()
+    kpm = None if inp.kpm is None else inp.kpm.cpu()
+    am = None if inp.am is None else inp.am.cpu()
+    t0 = time.perf_counter()
+    if w.rope_base is not None:
+        q = torch.from_numpy(oracle.rope(q, base=w.rope_base, round_to=w.dtype))
+        k = torch.from_numpy(oracle.rope(k, base=w.rope_base, round_to=w.dtype))
+    oracle.attention(q, k, v, causal=w.causal, kpm=kpm, am=am, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.d * visible_pairs(w, inp)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"the full workload {w.name}: all {w.B * w.H * w.T} rows, RoPE included when the "
+                      f"workload rotates, in {dt:.2f} s"}
 
 
 def reference_arm(args, w, rank, world):
@@ -218,16 +277,26 @@ def reference_arm(args, w, rank, world):
         return
     import oracle
     oracle.build()
-    g = torch.Generator().manual_seed(1000 + w.index)
-    shape = (1, 1, w.T, w.d)
-    qkv = []
-    for _ in range(3):
-        x = torch.randn(shape, generator=g) * w.std
-        qkv.append(x.to(w.torch_dtype).float())
+    kpm = am = None
+    if w.B * w.H * w.T * w.d <= (1 << 26):
+        # small workloads: the seeded inputs themselves, head (0, 0) with its masks
+        from blockwise_attention_gb300.workloads import make_inputs
+        inp = make_inputs(w, "cpu")
+        qkv = [x[0:1, 0:1].float() for x in (inp.q, inp.k, inp.v)]
+        kpm = None if inp.kpm is None else inp.kpm[0:1]
+        am = inp.am
+    else:
+        # one head of the same distribution (the full tensors take minutes to draw here)
+        g = torch.Generator().manual_seed(1000 + w.index)
+        shape = (1, 1, w.T, w.d)
+        qkv = []
+        for _ in range(3):
+            x = torch.randn(shape, generator=g) * w.std
+            qkv.append(x.to(w.torch_dtype).float())
     times, last = [], None
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        last = oracle_cpu_baseline(w, qkv, seconds=max(2.0, args.cpu_seconds / 2))
+        last = oracle_cpu_baseline(w, qkv, seconds=max(2.0, args.cpu_seconds / 2), kpm=kpm, am=am)
         if s >= args.warmup:
             times.append(time.perf_counter() - t0)
     value = last["value"]
@@ -332,7 +401,7 @@ def native_arm(args, w, rank, world, local_rank):
         # Independent groups of heads (B == 1) or batch items are pipelined over three
         # streams: host->device copy of group g+1 and device->host copy of group g-1
         # run while group g computes, each group one ring_attn_fwd call.
-        n_groups = 4
+        n_groups = 8
         if w.B == 1 and w.H % n_groups == 0:
             sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
         elif w.B % n_groups == 0:
@@ -399,16 +468,17 @@ def native_arm(args, w, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     attn_avg = statistics.mean(attn_ms)
     achieved = flops / (attn_avg * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": profiled_traffic(w.name), "kernel": f"attn_tc_kernel<{w.d}>",
-            "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a repeated step)",
-            "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"]),
-            "kernel_ms": attn_avg}
+    roof = tensor_roofline(achieved, peaks, peak_src, clocks, args.steps * ms_step / 1e3)
+    roof.update({"traffic": profiled_traffic(w.name), "kernel": f"attn_tc_kernel<{w.d}>", "kernel_ms": attn_avg})
     cpu = None
     if not args.no_cpu and world == 1 or (not args.no_cpu and rank == 0 and world == 1):
-        head = (inp.q[0:1, 0:1].float().cpu(), inp.k[0:1, 0:1].float().cpu(), inp.v[0:1, 0:1].float().cpu())
-        cpu = oracle_cpu_baseline(w, head, args.cpu_seconds)
+        if args.cpu_full:
+            cpu = oracle_full_baseline(w, inp)
+        else:
+            head = (inp.q[0:1, 0:1].float().cpu(), inp.k[0:1, 0:1].float().cpu(), inp.v[0:1, 0:1].float().cpu())
+            cpu = oracle_cpu_baseline(w, head, args.cpu_seconds,
+                                      kpm=None if inp.kpm is None else inp.kpm[0:1].cpu(),
+                                      am=None if inp.am is None else inp.am.cpu())
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -417,7 +487,7 @@ def native_arm(args, w, rank, world, local_rank):
                        "mode": args.mode, "visible_pairs": pairs, "flops_per_step": flops,
                        "l2": "inputs (Q, K, V: 1.6 GB) larger than the 129 MB L2; no flush"},
             "tokens_per_s": world * w.B * w.T / (ms_step * 1e-3),
-            "pct_of_bf16_peak": 100.0 * value / peak,
+            "pct_of_bf16_peak": 100.0 * value / roof["peak"],
             "rope_ms": statistics.mean(rope_ms),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": kernels_per_step * args.steps}
@@ -488,12 +558,11 @@ def backward_arm(args, w, rank, world, local_rank):
     tensor_path = w.torch_dtype == torch.bfloat16 and w.d in (64, 128)
     if tensor_path:
         peaks, src = load_peaks()
-        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-        roof = {"bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
-                "traffic": None, "kernel": "bwd_dkdv_tc_kernel + bwd_dq_tc_kernel",
-                "peak_source": f"{src} bf16_tflops_sustained; the kernels execute 14*d FLOP per pair (QK^T and "
-                               f"dout V^T are formed in both) against the 10*d counted",
-                "executed_frac": 1.4 * value / peak}
+        roof = tensor_roofline(value, peaks, src, clocks, args.steps * ms / 1e3)
+        roof.update({"traffic": None, "kernel": "bwd_dkdv_tc_kernel + bwd_dq_tc_kernel",
+                     "executed_frac": 1.4 * value / roof["peak"],
+                     "executed_note": "the kernels execute 14*d FLOP per pair (QK^T and dout V^T are formed in "
+                                      "both) against the 10*d counted"})
     else:
         peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": value, "peak": peak, "unit": "TFLOP/s", "frac": value / peak,
@@ -608,6 +677,64 @@ def ulysses_arm(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def merge_arm(args, w, rank, world, local_rank):
+    """Time attn_merge, the LSE merge of two fp32 partial attentions (the page's
+    accumulate_out_and_lse), over every row of the workload: (B*H*T, d) fp32
+    partials and (B*H*T) LSEs.  Bound by HBM: per row it reads both partials
+    and both LSEs and writes one of each, (3d + 3) * 4 bytes."""
+    import blockwise_attention_gb300 as ba
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    rows, d = w.B * w.H * w.T, w.d
+    g = torch.Generator(device=dev).manual_seed(3000 + w.index)
+    oa = torch.randn((rows, d), generator=g, device=dev)
+    ob = torch.randn((rows, d), generator=g, device=dev)
+    la = torch.randn((rows,), generator=g, device=dev) * 4
+    lb = torch.randn((rows,), generator=g, device=dev) * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ba.attn_merge(oa, la, ob, lb)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    nbytes = float(rows) * (3 * d + 3) * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {"metric": "LSE merge of partial attentions: HBM GB/s ((3d+3)*4 bytes per row)",
+            "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"merge_rows_of_{w.name}", "rows": rows, "d": d, "bytes_per_step": nbytes,
+                       "l2": f"partials ({2 * rows * d * 4 / 1e9:.2f} GB) far larger than the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "merge_kernel",
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms, "peak_source": f"{src} hbm_gbs (copy)"},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def decode_arm(args, rank, world, local_rank):
     """Time attn_decode_fwd on the decode workload (one query token per sequence,
     B=8, H=32, d=128, bf16, 64K-slot cache with ragged lengths).  Bound by HBM:
@@ -689,6 +816,8 @@ def main():
             ulysses_arm(args, w, rank, world, local_rank)
         elif args.variant == "decode":
             decode_arm(args, rank, world, local_rank)
+        elif args.variant == "merge":
+            merge_arm(args, w, rank, world, local_rank)
         else:
             native_arm(args, w, rank, world, local_rank)
     finally:

@@ -191,12 +191,31 @@ def _tensor(x: torch.Tensor) -> ba_tensor:
     return ba_tensor(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2))
 
 
-def _mask(m):
+def _mask(m, rows, cols, name="mask"):
+    """(pointer, ld) of a 2-D uint8 mask.  The library indexes masks at global
+    positions and sees only the pointer and the row stride, so the binding
+    checks here that the mask covers every row (batch item for the key-padding
+    mask, query position for attn_mask) and every key position a launch reads."""
     if m is None:
         return None, 0
-    if m.dtype != torch.uint8 or m.dim() != 2 or m.stride(1) != 1 or not m.is_cuda:
+    if m.dtype != torch.uint8 or m.dim() != 2 or m.stride(1) != 1:
+        raise ValueError("masks are 2-D uint8 CUDA tensors with a contiguous last axis")
+    if m.shape[0] < rows or m.shape[1] < cols:
+        raise ValueError(f"{name} of shape {tuple(m.shape)} does not cover the ({rows}, {cols}) "
+                         f"rows and key positions the call reads")
+    if m.shape[0] > 1 and m.stride(0) < cols:
+        raise ValueError(f"{name} rows overlap (stride {m.stride(0)} < {cols} key positions)")
+    if not m.is_cuda:
         raise ValueError("masks are 2-D uint8 CUDA tensors with a contiguous last axis")
     return ctypes.c_void_p(m.data_ptr()), m.stride(0)
+
+
+def _masks(key_padding_mask, attn_mask, B, q_rows, k_cols):
+    """Both masks of a call whose queries reach global position q_rows - 1 and
+    whose keys reach k_cols - 1."""
+    kpm, kpm_ld = _mask(key_padding_mask, B, k_cols, "key_padding_mask")
+    am, am_ld = _mask(attn_mask, q_rows, k_cols, "attn_mask")
+    return kpm, kpm_ld, am, am_ld
 
 
 def _ptr(t):
@@ -226,8 +245,7 @@ def attn_block_fwd(q, k, v, *, q_off=0, k_off=0, key_padding_mask=None, attn_mas
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
     _check_out(out, lse, (B, H, Lq, d))
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, q_off + Lq, k_off + Lk)
     need = lib.attn_block_fwd_workspace_size(B, Lq, Lk, int(kpm is not None or am is not None))
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -248,8 +266,7 @@ def attn_block_fwd_noalloc(q, k, v, out, lse, *, q_off=0, k_off=0, key_padding_m
     B, H, Lq, d = q.shape
     Lk = k.shape[2]
     _check_out(out, lse, (B, H, Lq, d))
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, q_off + Lq, k_off + Lk)
     rc = lib.attn_block_fwd_noalloc(_tensor(q), _tensor(k), _tensor(v), B, H, Lq, Lk, d, _dtype_code(q.dtype),
                                     q_off, k_off, kpm, kpm_ld, am, am_ld, int(bool(causal)),
                                     0.0 if scale is None else float(scale), _ptr(out), _dtype_code(out.dtype),
@@ -297,8 +314,7 @@ def ring_attn_fwd(q, k, v, *, P, partition="contiguous", mode="fused", key_paddi
     if lse is None:
         lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     _check_out(out, lse, (B, H, T, d))
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, T, T)
     masks = kpm is not None or am is not None
     need = ring_attn_fwd_workspace_size(B, H, T, d, q.dtype, P, partition, mode, masks, rope, out.dtype)
     if workspace is None and need:
@@ -351,8 +367,7 @@ def attn_block_bwd(q, k, v, out, dout, lse, *, q_off=0, k_off=0, key_padding_mas
     Lk = k.shape[2]
     _check_bwd_inputs(q, out, dout, lse)
     dq, dk, dv = _grads(B, H, Lq, Lk, d, q.device, dq, dk, dv)
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, q_off + Lq, k_off + Lk)
     need = lib.attn_block_bwd_workspace_size(B, H, Lq)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -374,8 +389,7 @@ def ring_attn_bwd(q, k, v, out, dout, lse, *, P, partition="contiguous", mode="f
     B, H, T, d = q.shape
     _check_bwd_inputs(q, out, dout, lse)
     dq, dk, dv = _grads(B, H, T, T, d, q.device, dq, dk, dv)
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, T, T)
     need = lib.ring_attn_bwd_workspace_size(B, H, T)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -436,8 +450,7 @@ def ulysses_attn_fwd(q_tok, k_tok, v_tok, *, key_padding_mask=None, attn_mask=No
         raise ValueError("out must be contiguous, of the shape and dtype of q_tok")
     if tuple(lse.shape) != (P, H, B, Tl) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 tensor of shape (P, H, B, T/P)")
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, T, T)
     dt = _dtype_code(q_tok.dtype)
     need = lib.ulysses_attn_fwd_workspace_size(P, H, B, T, d, dt, int(kpm is not None or am is not None))
     if workspace is None and need:
@@ -505,8 +518,7 @@ def tile_classes(B, Lq, Lk, *, q_off=0, k_off=0, key_padding_mask=None, attn_mas
     """int8 (B, ceil(Lq/128), ceil(Lk/128)) tile classes computed on the device."""
     lib = load()
     out = torch.empty((B, -(-Lq // 128), -(-Lk // 128)), dtype=torch.int8, device=device)
-    kpm, kpm_ld = _mask(key_padding_mask)
-    am, am_ld = _mask(attn_mask)
+    kpm, kpm_ld, am, am_ld = _masks(key_padding_mask, attn_mask, B, q_off + Lq, k_off + Lk)
     _check("ba_tile_classes", lib.ba_tile_classes(B, Lq, Lk, q_off, k_off, kpm, kpm_ld, am, am_ld,
                                                   int(bool(causal)), _ptr(out), _stream(stream)))
     return out

@@ -13,6 +13,12 @@
  *  - Masks are uint8 with 1 = EXCLUDED, indexed at GLOBAL token positions:
  *      key_padding_mask[b * kpm_ld + key_pos]      (B rows, >= total keys)
  *      attn_mask[query_pos * am_ld + key_pos]      (>= total queries rows)
+ *    The library receives only the pointer and the row stride, so it cannot
+ *    see how many rows a mask has: the caller must pass a key-padding mask
+ *    with at least B rows and an attn_mask with a row for every global query
+ *    position of the call (q_off + Lq rows for a block, T for a ring), each
+ *    row covering every global key position the call reads.  A shorter mask
+ *    is read past its end.  (The Python binding checks the shapes.)
  *    A pair (i, j) takes part iff it is not excluded by causality (j > i,
  *    when causal != 0), by the key padding of its batch item, or by attn_mask:
  *    the exclusions are OR-combined ("PyTorch MultiheadAttention", item #2 of
@@ -371,7 +377,10 @@ int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int 
  *    returns BA_ERR_NOALLOC_LIMIT before launching anything.
  *  - The first call on a device looks up the array's device address on that
  *    device (cudaGetSymbolAddress); make that first call before any stream
- *    capture.
+ *    capture.  The address is kept for the rest of the process, so a
+ *    cudaDeviceReset() of that device after the first call is not supported
+ *    (the reset unloads the module and the kept address would be stale; the
+ *    library's timeout flag is looked up and kept the same way).
  *  - All calls on a GPU share that GPU's array, and it keeps the last call's
  *    contents.  Every entry a call reads is first written by that call, so
  *    nothing needs clearing; but calls that overlap on the same GPU (for

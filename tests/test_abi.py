@@ -105,3 +105,25 @@ def test_workspace_sizes():
                                            "stepwise", False, False) == 256
     assert ba.ring_attn_fwd_workspace_size(1, 1, 128 * 65, 64, __import__("torch").float32, 65, "contiguous",
                                            "stepwise", False, False) == 512
+
+
+def test_masks_must_cover_the_positions_read():
+    """The C ABI sees only a mask's pointer and row stride; the binding rejects a
+    mask with too few rows or key positions before any launch (a local (Lq, Lk)
+    attn_mask passed with q_off > 0 is the easy way to get this wrong)."""
+    import torch
+    kpm = torch.zeros((2, 100), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="does not cover"):
+        _lib._masks(kpm, None, 3, 10, 100)            # fewer rows than batch items
+    with pytest.raises(ValueError, match="does not cover"):
+        _lib._masks(kpm, None, 2, 10, 101)            # fewer key positions than k_off + Lk
+    am = torch.zeros((64, 128), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="does not cover"):
+        _lib._masks(None, am, 1, 32 + 64, 128)        # local (Lq, Lk) mask with q_off = 32
+    with pytest.raises(ValueError, match="overlap"):
+        _lib._masks(None, torch.zeros((4, 256), dtype=torch.uint8)[:, :100].as_strided((8, 100), (50, 1)),
+                    1, 8, 100)
+    # shapes that cover everything pass the coverage checks (and stop only at the
+    # device check, since these are host tensors)
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib._masks(kpm, am, 2, 64, 100)

@@ -91,3 +91,26 @@ def test_encoder_pad_band_512(mode):
     cls = ba.tile_classes(w.B, w.T, w.T, key_padding_mask=inp.kpm, attn_mask=inp.am).cpu().numpy()
     ref = oracle.tile_classes(2, w.T, w.T, kpm=inp.kpm[:2].cpu().numpy(), am=inp.am.cpu().numpy())
     assert np.array_equal(cls[:2], ref)
+
+
+@pytest.mark.parametrize("mode", ["fused", "stepwise"])
+def test_zigzag_prefill_64k_peaked(mode):
+    """The 64K workload with Q scaled by 16 (exact in bf16): scores of standard
+    deviation about 4, so each row's softmax is dominated by a few keys and |O|
+    stays near the size of one V row on every row, late rows included.  A row
+    that was zeroed, or that folded in the wrong V tile, fails here; with the
+    plain workload most late rows average thousands of values toward zero and
+    sit below the absolute bound.  Both ring modes, RoPE inside the call."""
+    w = WORKLOADS["zigzag_prefill_64k_rope"]
+    inp = make_inputs(w, "cuda")
+    inp = type(inp)(inp.q * 16, inp.k, inp.v, inp.lengths, inp.kpm, inp.am)
+    out, lse = run_ring(w, inp, mode)
+    heads = [(0, 3), (0, 22)]
+    rows_r = sample_rows(len(heads), 1, w.T, [(i, 0) for i in range(len(heads))], 192, w.T // (2 * w.P),
+                         seed=5)
+    o_ref, l_ref = oracle_ring_reference(inp, w, rows=rows_r, heads=heads)
+    sel_o = torch.stack([out[b, h] for b, h in heads]).reshape(-1, w.d)[torch.from_numpy(rows_r).cuda()]
+    sel_l = torch.stack([lse[b, h] for b, h in heads]).reshape(-1)[torch.from_numpy(rows_r).cuda()]
+    stats = compare(sel_o, sel_l, o_ref, l_ref, "bf16", f"zigzag_prefill_64k peaked {mode}")
+    # the absolute bound can fail on (almost) every sampled row of this input
+    assert stats["rows_below_abs_tol"] < 0.02, stats

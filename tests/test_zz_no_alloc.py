@@ -9,18 +9,19 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import blockwise_attention_gb300 as ba
 from blockwise_attention_gb300 import _lib
-from tests.parity import TOL_LSE, TOL_OUT
+from tests.parity import TOL_LSE, TOL_OUT, compare
 
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(B, H, Lq, Lk, d, seed):
+def _inputs(B, H, Lq, Lk, d, seed, dtype=torch.bfloat16):
     g = torch.Generator(device="cuda").manual_seed(seed)
-    q = torch.randn((B, H, Lq, d), generator=g, device="cuda").to(torch.bfloat16)
-    k = torch.randn((B, H, Lk, d), generator=g, device="cuda").to(torch.bfloat16)
-    v = torch.randn((B, H, Lk, d), generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((B, H, Lq, d), generator=g, device="cuda").to(dtype)
+    k = torch.randn((B, H, Lk, d), generator=g, device="cuda").to(dtype)
+    v = torch.randn((B, H, Lk, d), generator=g, device="cuda").to(dtype)
     rng = np.random.default_rng(seed)
     kpm = np.zeros((B, Lk), np.uint8)
     for b in range(B):
@@ -32,13 +33,17 @@ def _inputs(B, H, Lq, Lk, d, seed):
     return q, k, v, torch.from_numpy(kpm).cuda(), torch.from_numpy(am).cuda()
 
 
-def _check_same(out_n, lse_n, out_r, lse_r):
+def _check_same(out_n, lse_n, out_r, lse_r, dt="bf16"):
     o_n, o_r = out_n.float().cpu().numpy(), out_r.float().cpu().numpy()
     l_n, l_r = lse_n.cpu().numpy(), lse_r.cpu().numpy()
     fin = np.isfinite(l_r)
     assert np.array_equal(fin, np.isfinite(l_n))
-    assert np.max(np.abs(o_n - o_r)) <= TOL_OUT["bf16"]
+    assert np.max(np.abs(o_n - o_r)) <= TOL_OUT[dt]
     assert np.max(np.abs(l_n[fin] - l_r[fin])) <= TOL_LSE
+
+
+def _oracle(q, k, v, **kw):
+    return oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), **kw)
 
 
 def test_noalloc_matches_attn_block_fwd_on_two_calls():
@@ -56,6 +61,55 @@ def test_noalloc_matches_attn_block_fwd_on_two_calls():
         assert ba.sync_status() == 0
         _check_same(out_n, lse_n, out_r, lse_r)
         assert torch.all(lse_n[:, :, 7] == -math.inf)
+        # and against the fp64 oracle on the same inputs
+        o_ref, l_ref = _oracle(q, k, v, causal=causal, kpm=kpm.cpu().numpy(), am=am.cpu().numpy(),
+                               q_pos0=Lk - Lq)
+        compare(out_n, lse_n, o_ref, l_ref, "bf16", f"noalloc B={B} Lq={Lq} Lk={Lk} causal={causal}")
+
+
+@pytest.mark.parametrize("dt,d", [("f32", 64), ("bf16", 32), ("f32", 16)])
+def test_noalloc_cuda_core_path(dt, d):
+    """fp32 inputs and bf16 with d = 32 run on the CUDA-core kernel, which reads
+    the same fixed tile-class array; two calls in a row, masked then masked
+    with other shapes, against attn_block_fwd and the oracle."""
+    dtype = torch.float32 if dt == "f32" else torch.bfloat16
+    for (B, H, Lq, Lk, causal, seed) in [(2, 3, 260, 390, True, 21), (3, 2, 140, 333, False, 22)]:
+        q, k, v, kpm, am = _inputs(B, H, Lq, Lk, d, seed, dtype)
+        out_r, lse_r = ba.attn_block_fwd(q, k, v, q_off=Lk - Lq, key_padding_mask=kpm, attn_mask=am,
+                                         causal=causal, out_dtype=torch.float32)
+        out_n = torch.empty_like(out_r)
+        lse_n = torch.empty_like(lse_r)
+        ba.attn_block_fwd_noalloc(q, k, v, out_n, lse_n, q_off=Lk - Lq, key_padding_mask=kpm, attn_mask=am,
+                                  causal=causal)
+        torch.cuda.synchronize()
+        assert ba.sync_status() == 0
+        _check_same(out_n, lse_n, out_r, lse_r, dt)
+        o_ref, l_ref = _oracle(q, k, v, causal=causal, kpm=kpm.cpu().numpy(), am=am.cpu().numpy(),
+                               q_pos0=Lk - Lq)
+        compare(out_n, lse_n, o_ref, l_ref, dt, f"noalloc {dt} d={d} causal={causal}")
+
+
+def test_noalloc_without_masks_and_accumulate():
+    """Causal without masks (no class map: the kernel deals work items
+    round-robin), then a second key block merged into the first with
+    accumulate=1 into an fp32 out; both against attn_block_fwd and the oracle."""
+    B, H, Lq, d = 2, 4, 384, 128
+    q, k, v, _, _ = _inputs(B, H, Lq, 700, d, 31)
+    k0, v0, k1, v1 = k[:, :, :316], v[:, :, :316], k[:, :, 316:], v[:, :, 316:]
+    q_off = 700 - Lq
+    out_r, lse_r = ba.attn_block_fwd(q, k0, v0, q_off=q_off, causal=True, out_dtype=torch.float32)
+    out_n = torch.empty_like(out_r)
+    lse_n = torch.empty_like(lse_r)
+    ba.attn_block_fwd_noalloc(q, k0, v0, out_n, lse_n, q_off=q_off, causal=True)
+    torch.cuda.synchronize()
+    _check_same(out_n, lse_n, out_r, lse_r)
+    ba.attn_block_fwd(q, k1, v1, q_off=q_off, k_off=316, causal=True, out=out_r, lse=lse_r, accumulate=True)
+    ba.attn_block_fwd_noalloc(q, k1, v1, out_n, lse_n, q_off=q_off, k_off=316, causal=True, accumulate=True)
+    torch.cuda.synchronize()
+    assert ba.sync_status() == 0
+    _check_same(out_n, lse_n, out_r, lse_r)
+    o_ref, l_ref = _oracle(q, k, v, causal=True, q_pos0=q_off)
+    compare(out_n, lse_n, o_ref, l_ref, "bf16", "noalloc causal + accumulate")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():

@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    ap.add_argument("--partition", default=None, choices=["contiguous", "zigzag", "striped"],
+                    help="override the workload's partition of the P ranks")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -801,6 +803,8 @@ def main():
     args = parse()
     from blockwise_attention_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.partition:
+        w = w.replace(partition=args.partition)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

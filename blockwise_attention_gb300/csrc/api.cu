@@ -110,6 +110,22 @@ int encode_map(CUtensorMap *m, const void *base, int d, long long rows, int H, i
     return r == CUDA_SUCCESS ? BA_OK : BA_ERR_CUDA;
 }
 
+// Striped ring: the (B, H, T, d) tensor seen as {d, P, T/P, H, B}, token
+// r + P u at coordinates (r, u), so that a box {64, 1, 128, 1, 1} loads 128
+// consecutive tokens of rank r (a stride of P rows) into the same shared-memory
+// layout as the 4-D box.
+int encode_map_striped(CUtensorMap *m, const void *base, int d, int P, long long T, int H, int B, long long sT,
+                       long long sH, long long sB) {
+    cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)P, (cuuint64_t)(T / P), (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)sT * 2, (cuuint64_t)sT * 2 * P, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
+    cuuint32_t box[5] = {64, 1, (cuuint32_t)TILE, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BA_OK : BA_ERR_CUDA;
+}
+
 // TMA needs 16-byte aligned bases and byte strides; B or H of 1 may carry any stride.
 bool tma_ok(const ba_tensor &t, int B, int H) {
     auto al = [](long long s) { return (s * 2) % 16 == 0 && s >= 0; };
@@ -500,6 +516,13 @@ int run_attention(AttnArgs &a, int dev, int nrows_q, int nrows_k, cudaStream_t s
     if (rc) return rc;
     TmaMaps m;
     const int B = a.g.B, H = a.g.H, d = a.g.d;
+    if (a.g.striped) {
+        const int P = a.g.P;
+        if ((rc = encode_map_striped(&m.q, a.q, d, P, nrows_q, H, B, a.qsT, a.qsH, a.qsB))) return rc;
+        if ((rc = encode_map_striped(&m.k, a.k, d, P, nrows_k, H, B, a.ksT, a.ksH, a.ksB))) return rc;
+        if ((rc = encode_map_striped(&m.v, a.v, d, P, nrows_k, H, B, a.vsT, a.vsH, a.vsB))) return rc;
+        return launch_attn_tc(a, m, g_num_sms[dev], s);
+    }
     if ((rc = encode_map(&m.q, a.q, d, nrows_q, H, B, a.qsT, a.qsH, a.qsB))) return rc;
     if ((rc = encode_map(&m.k, a.k, d, nrows_k, H, B, a.ksT, a.ksH, a.ksB))) return rc;
     if ((rc = encode_map(&m.v, a.v, d, nrows_k, H, B, a.vsT, a.vsH, a.vsB))) return rc;
@@ -533,7 +556,8 @@ const char *ba_strerror(int code) {
 int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int num_sms, int32_t *items,
                      int64_t capacity) {
     if (B < 0 || H < 0 || T < 0 || P < 1 || num_sms < 1 || capacity < 0) return BA_ERR_ARG;
-    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG && partition != BA_PART_STRIPED)
+        return BA_ERR_ARG;
     const int NC = partition == BA_PART_ZIGZAG ? 2 * P : P;
     if (T % NC) return BA_ERR_SHAPE;
     if ((long long)B * H == 0 || T == 0) return 0;
@@ -544,6 +568,7 @@ int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int 
     g.H = H;
     g.d = 128;
     g.ring = 1;
+    g.striped = partition == BA_PART_STRIPED;
     g.T = T;
     g.P = P;
     g.zigzag = partition == BA_PART_ZIGZAG;
@@ -793,8 +818,10 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     if (B < 0 || H < 0 || T < 0 || P < 1 || !valid_dtype(dtype)) return BA_ERR_ARG;
     if ((long long)B * H * T > 0 && (check_tensor(q) || check_tensor(k) || check_tensor(v) || !out || !lse))
         return BA_ERR_ARG;
-    if (partition == BA_PART_STRIPED) return BA_ERR_UNSUPPORTED;   // tokens of a rank are not a position range
-    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG) return BA_ERR_ARG;
+    if (partition != BA_PART_CONTIGUOUS && partition != BA_PART_ZIGZAG && partition != BA_PART_STRIPED)
+        return BA_ERR_ARG;
+    // striped: masks are indexed by token, and a rank's tokens are not a range of them
+    if (partition == BA_PART_STRIPED && (key_padding_mask || attn_mask)) return BA_ERR_UNSUPPORTED;
     if (mode != BA_MODE_STEPWISE && mode != BA_MODE_FUSED) return BA_ERR_ARG;
     if (out_dtype != BA_F32 && out_dtype != dtype) return BA_ERR_ARG;
     if (!valid_d(d)) return BA_ERR_SHAPE;
@@ -835,6 +862,7 @@ int ring_attn_fwd(ba_tensor q, ba_tensor k, ba_tensor v, int B, int H, int T, in
     g.H = H;
     g.d = d;
     g.ring = 1;
+    g.striped = partition == BA_PART_STRIPED;
     g.T = T;
     g.P = P;
     g.zigzag = partition == BA_PART_ZIGZAG;

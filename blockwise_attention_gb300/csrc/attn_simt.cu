@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
     float q[D], o[D];
 #pragma unroll
     for (int c = 0; c < D; ++c) {
-        q[c] = valid ? to_f32(qb[(long long)(qt.row0 + r) * a.qsT + c]) : 0.f;
+        q[c] = valid ? to_f32(qb[row_token(g, qt.row0 + r) * a.qsT + c]) : 0.f;
         o[c] = 0.f;
     }
     float m = -INFINITY, l = 0.f;   // running max (log2 units) and denominator
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
             for (int e = threadIdx.x; e < SUB * D; e += blockDim.x) {
                 int j = e / D, c = e % D;
                 bool in = s0 + j < kt.len;
-                long long row = kt.row0 + s0 + j;
+                long long row = g.ring ? row_token(g, kt.row0 + s0 + j) : kt.row0 + s0 + j;
                 Ks[j][c] = in ? to_f32(kb[row * a.ksT + c]) : 0.f;
                 Vs[j][c] = in ? to_f32(vb[row * a.vsT + c]) : 0.f;
             }
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
         }
     }
     if (!valid) return;
-    const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + qt.row0 + r;
+    const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row(g, qt, r);
     const float acc_l = a.acc_lse ? a.acc_lse[row_flat] : -INFINITY;
     const RowFinal f = row_final(m, l, acc_l);
 #pragma unroll

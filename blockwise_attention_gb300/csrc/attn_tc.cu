@@ -254,11 +254,11 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 mbar_arrive_expect_tx(bar(C::B_QFULL), (has1 ? 2 : 1) * C::TILE_BYTES);
                 for (int bx = 0; bx < C::NBOX; ++bx)
-                    tma_load_4d(sQ + bx * C::BOX_BYTES, &tq, bx * 64, p.q0.row0, p.q0.h, p.q0.b, bar(C::B_QFULL));
+                    tma_load_rows(sQ + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q0.row0, p.q0.h, p.q0.b, bar(C::B_QFULL));
                 if (has1)
                     for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_4d(sQ + C::TILE_BYTES + bx * C::BOX_BYTES, &tq, bx * 64, p.q1.row0, p.q0.h, p.q0.b,
-                                    bar(C::B_QFULL));
+                        tma_load_rows(sQ + C::TILE_BYTES + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q1.row0, p.q0.h,
+                                      p.q0.b, bar(C::B_QFULL));
                 ++qfills;
                 KWalk wk;
                 kwalk_begin(g, p.span, wk);
@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_4d(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, bx * 64, kt.row0, p.q0.h,
-                                        p.q0.b, bar(C::B_KFULL + st));
+                            tma_load_rows(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, g, bx * 64, kt.row0,
+                                          p.q0.h, p.q0.b, bar(C::B_KFULL + st));
                         ++kfill;
                     }
                     if (prev_row >= 0) {
@@ -297,8 +297,8 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_4d(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, bx * 64, prev_row, p.q0.h,
-                                        p.q0.b, bar(C::B_VFULL + st));
+                            tma_load_rows(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, g, bx * 64, prev_row,
+                                          p.q0.h, p.q0.b, bar(C::B_VFULL + st));
                         ++vfill;
                     }
                     if (!more) break;
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(320, 1)
             ++ox;
             tc_fence_after();
             const bool valid = row < qt.len;
-            const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + qt.row0 + row;
+            const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row(g, qt, row);
             const float acc_l = (a.acc_lse != nullptr && valid) ? a.acc_lse[row_flat] : -INFINITY;
             const RowFinal f = row_final(m_ref, n > 0 ? l : 0.f, acc_l);
 #pragma unroll

@@ -30,9 +30,23 @@ constexpr float LN2 = 0.6931471805599453f;
 // whose length is not a multiple of 128 ends in a ragged tile.  A query tile
 // of rank r visits, for ring steps s in [s_begin, s_end), the key tiles of the
 // chunks of rank (r - s) mod P in that rank's local order.
+//
+// Striped ring (striped = 1; brunomaga "When to use Ulysses and Ring
+// attention" names Striped Attention): rank r owns the tokens t = r + P u,
+// u = 0 .. CL-1 (NC = P, CL = T / P).  The walk then runs over "rows" in rank
+// order, R = r CL + u, whose token is r + P u (row_token below): the tensor
+// maps address the rows of a rank as a strided view, and out / lse are stored
+// at the tokens.  Causality needs no global position: key (rank c, local u')
+// is visible to query (rank r, local u) iff c + P u' <= r + P u, i.e. iff
+// u' <= u when c <= r and u' < u when c > r.  So the walk's positions are
+// local indices, a query at u and a key at u' + [c > r]: the block of every
+// (rank, step) pair is the lower triangle with its diagonal (c <= r) or
+// without it (c > r), and "key position <= query position" holds as in the
+// other partitions.  Masks are indexed by token and are not taken here.
 struct Geom {
     int B, H, d;
     int ring;
+    int striped;
     // block mode
     int Lq, Lk;
     long long q_off, k_off;
@@ -86,7 +100,7 @@ __host__ __device__ inline QTile q_tile(const Geom &g, int qg, int b, int h) {
         t.row0 = c * g.CL + i * TILE;
         int end = (c + 1) * g.CL;
         t.len = (t.row0 + TILE < end ? t.row0 + TILE : end) - t.row0;
-        t.pos0 = t.row0;
+        t.pos0 = g.striped ? i * TILE : t.row0;   // striped: local index within the rank
         t.rank = chunk_owner(g, c);
     } else {
         t.row0 = qg * TILE;
@@ -132,18 +146,28 @@ struct KWalk {
     int q_last;     // global position of the query tile's last row
     int q_first;    // global position of the query tile's first row
     int pos_off;    // global position = row + pos_off
+    int qrank;      // rank of the query tile (ring mode)
 };
+
+// Position of the first key of chunk c for a query tile of rank qrank: its
+// global position, or in the striped ring its local index 0 shifted by one
+// when the key's rank follows the query's (see Geom).
+__host__ __device__ __forceinline__ int chunk_pos0(const Geom &g, int c, int qrank) {
+    return g.striped ? (c > qrank ? 1 : 0) : c * g.CL;
+}
 
 __host__ __device__ __forceinline__ void kwalk_set_chunk(const Geom &g, KWalk &w, int c) {
     w.row = c * g.CL;
     w.chunk_end = w.row + g.CL;
     w.idx = c * g.nkt_pc;
+    w.pos_off = chunk_pos0(g, c, w.qrank) - w.row;
 }
 
 __host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile &q, KWalk &w) {
     w.q_first = (int)q.pos0;
     w.q_last = (int)q.pos0 + q.len - 1;
     w.ci = 0;
+    w.qrank = q.rank;
     if (g.ring) {
         w.pos_off = 0;
         w.s = g.s_begin;
@@ -240,11 +264,24 @@ __host__ __device__ inline int kwalk_count(const Geom &g, const QTile &q) {
     int n = 0;
     int src = ((q.rank - g.s_begin) % g.P + g.P) % g.P;
     for (int s = g.s_begin; s < g.s_end; ++s) {
-        n += chunk_tiles((long long)src * g.CL, g.CL);
-        if (g.zigzag) n += chunk_tiles((long long)(2 * g.P - 1 - src) * g.CL, g.CL);
+        n += chunk_tiles(chunk_pos0(g, src, q.rank), g.CL);
+        if (g.zigzag) n += chunk_tiles(chunk_pos0(g, 2 * g.P - 1 - src, q.rank), g.CL);
         src = src == 0 ? g.P - 1 : src - 1;
     }
     return n;
+}
+
+// Token of row R of a ring tensor: R itself, or r + P u for row R = r CL + u
+// of the striped ring.
+__host__ __device__ __forceinline__ long long row_token(const Geom &g, long long R) {
+    if (!g.striped) return R;
+    const long long r = R / g.CL;
+    return r + (long long)g.P * (R - r * g.CL);
+}
+
+// Row of out / lse (token order) for row `row` of query tile q.
+__host__ __device__ __forceinline__ long long out_row(const Geom &g, const QTile &q, int row) {
+    return g.striped ? q.rank + (long long)g.P * (q.pos0 + row) : (long long)q.row0 + row;
 }
 
 // Work item w -> (q tile, b, h).  Items are grouped by heads_per_group (b, h)
@@ -320,9 +357,18 @@ __host__ __device__ inline QPair work_pair(const Geom &g, int w) {
         pi = heavy + w2 / BH;
         bh = w2 % BH;
     }
-    const int pg = g.causal ? np - 1 - pi : pi;
     const int ppc = pairs_per_chunk(g), per = g.ring ? g.nqt_pc : g.n_qtiles;
-    const int c = pg / ppc, i = pg % ppc;
+    int c, i;
+    if (g.striped && g.causal) {
+        // a query at local index u of rank r sees P u + r + 1 keys: deal the
+        // levels of all ranks together, last level and last rank first
+        c = g.NC - 1 - pi % g.NC;
+        i = ppc - 1 - pi / g.NC;
+    } else {
+        const int pg = g.causal ? np - 1 - pi : pi;
+        c = pg / ppc;
+        i = pg % ppc;
+    }
     const int b = bh / g.H, h = bh % g.H;
     QPair p;
     p.q0 = q_tile(g, c * per + 2 * i, b, h);

@@ -26,6 +26,28 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// 128 rows of 64 columns starting at row R of head (h, b): a 4-D box at row R,
+// or, in the striped ring, a 5-D box {64, 1, 128, 1, 1} over the view
+// {d, P, CL, H, B} (row R = r CL + u is token r + P u: coordinates (r, u)).
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, const Geom &g, int col, int R,
+                                              int h, int b, uint32_t bar) {
+    if (g.striped) {
+        const int r = R / g.CL;
+        tma_load_5d(dst, map, col, r, R - r * g.CL, h, b, bar);
+    } else {
+        tma_load_4d(dst, map, col, R, h, b, bar);
+    }
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 version field.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |

@@ -71,9 +71,12 @@ enum {
 
 enum { BA_F32 = 0, BA_BF16 = 1 };
 /* Token partitions over P ranks: contiguous blocks, zigzag (2P chunks, rank r
- * holds chunks r and 2P-1-r), and striped (token t on rank t mod P; index maps
- * only: ring_attn_fwd / ring_attn_bwd return BA_ERR_UNSUPPORTED for it, since a
- * rank's tokens are not a range of positions). */
+ * holds chunks r and 2P-1-r), and striped (token t on rank t mod P, rank r
+ * holding r, r+P, r+2P, ... in that order; brunomaga "When to use Ulysses and
+ * Ring attention" names Striped Attention).  ring_attn_fwd takes striped
+ * partitions without masks (masks are indexed by token, and a striped rank's
+ * tokens are not a range: BA_ERR_UNSUPPORTED with a mask); ring_attn_bwd
+ * returns BA_ERR_UNSUPPORTED for them. */
 enum { BA_PART_CONTIGUOUS = 0, BA_PART_ZIGZAG = 1, BA_PART_STRIPED = 2 };
 enum { BA_MODE_STEPWISE = 0, BA_MODE_FUSED = 1 };
 enum { BA_TILE_EMPTY = 0, BA_TILE_FULL = 1, BA_TILE_PARTIAL = 2 };
@@ -137,7 +140,10 @@ int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_
  * "Distributed algorithm").  The T tokens are split into P ranks
  * (partition = BA_PART_CONTIGUOUS: P equal time blocks; BA_PART_ZIGZAG: 2P
  * equal chunks, rank r owning chunks r and 2P-1-r, llm-systems "Balance the
- * workload in causal attention").  Every rank keeps its queries resident; at
+ * workload in causal attention"; BA_PART_STRIPED: rank r owns the tokens
+ * r + P u, and under causal masking its block against the K/V of rank c is a
+ * lower triangle over local indices, with the diagonal when c <= r and
+ * without it when c > r).  Every rank keeps its queries resident; at
  * ring step s = 0..P-1 it folds in the K/V block of rank (r - s) mod P (local
  * block first, then the previous rank's, ...).  Positions and masks stay the
  * global ones.  There is no inter-GPU traffic: each rank's "received" block is
@@ -154,8 +160,9 @@ int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_
  *  lse: (B, H, T) fp32.
  *  index_maps_out: NULL, or host int32[T + P*P] receiving the partition
  *    (rank-major token ids, P x T/P) followed by the schedule src[r][s].
- * Errors: BA_ERR_SHAPE when T is not divisible by P (contiguous) or 2P
- * (zigzag), or d is unsupported; BA_ERR_ARG as for attn_block_fwd.
+ * Errors: BA_ERR_SHAPE when T is not divisible by P (contiguous, striped) or
+ * 2P (zigzag), or d is unsupported; BA_ERR_UNSUPPORTED for a striped
+ * partition with a mask; BA_ERR_ARG as for attn_block_fwd.
  */
 size_t ring_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype, int P,
                                     int partition, int mode, int has_masks, int rope,

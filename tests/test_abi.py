@@ -77,9 +77,14 @@ def test_argument_errors_are_host_side():
     assert lib.rope_apply(T1, T0, 1, 1, 8, 7, 1, None, 1e4, 1.0, dummy, None, None) == _lib.BA_ERR_ARG
     # negative Position Interpolation scale
     assert lib.rope_apply(T1, T0, 1, 1, 8, 8, 1, None, 1e4, -0.5, dummy, None, None) == _lib.BA_ERR_ARG
-    # striped partitions have index maps but no ring kernel
-    assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 16, 64, 1, 4, 2, 1, None, 0, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
+    # striped partitions take no masks (masks are indexed by token); T must divide by P
+    assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 16, 64, 1, 4, 2, 1, dummy, 16, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
                              dummy, None, None, 0, None) == _lib.BA_ERR_UNSUPPORTED
+    assert lib.ring_attn_fwd(T1, T1, T1, 1, 1, 18, 64, 1, 4, 2, 1, None, 0, None, 0, 1, 0.0, 0, 1e4, dummy, 1,
+                             dummy, None, None, 0, None) == _lib.BA_ERR_SHAPE
+    # the striped backward is not built
+    assert lib.ring_attn_bwd(T1, T1, T1, T1, T1, dummy, 1, 1, 16, 64, 1, 4, 2, 1, None, 0, None, 0, 1, 0.0,
+                             dummy, dummy, dummy, None, 0, None) == _lib.BA_ERR_UNSUPPORTED
     assert lib.attn_merge(None, dummy, dummy, dummy, 4, 4, None) == _lib.BA_ERR_ARG
     # backward: NULL out, unsupported d, T not divisible by 2P, masks not covering positions
     assert lib.attn_block_bwd(T1, T1, T1, T0, T1, dummy, 1, 1, 8, 8, 64, 1, 0, 0, None, 0, None, 0, 0, 0.0,

@@ -20,14 +20,32 @@ CASES = [
     (2, 3, 1000, 4, "contiguous", False, 152),  # bidirectional
     (1, 2, 384, 3, "zigzag", True, 4),          # 64-token chunks, few SMs
     (3, 5, 2560, 2, "contiguous", True, 16),    # 10 tiles per chunk
+    (4, 16, 8192, 8, "striped", True, 152),     # 8K prefill shapes, striped ranks
+    (2, 3, 1000, 4, "striped", True, 152),      # 250-token ranks: one ragged tile each
+    (1, 2, 384, 3, "striped", True, 4),         # 128-token ranks
+    (2, 2, 1024, 4, "striped", False, 16),      # bidirectional
 ]
 
 
 def query_tiles(T, P, partition):
-    """(row0, rows) of every 128-row query tile: tiles are cut from each chunk start."""
+    """(row0, rows) of every 128-row query tile: tiles are cut from each chunk start.
+    Rows are token positions, except for striped ranks, whose rows are in rank
+    order: row c * cl + u holds token c + P * u."""
     nc = 2 * P if partition == "zigzag" else P
     cl = T // nc
     return [(c * cl + r, min(128, cl - r)) for c in range(nc) for r in range(0, cl, 128)], cl
+
+
+def tile_visible(T, P, partition, q_row0, q_rows, k_row0, k_rows):
+    """Does any key of the key tile precede or equal any query of the query tile
+    (causal), by the tokens themselves?"""
+    if partition != "striped":
+        return k_row0 <= q_row0 + q_rows - 1
+    cl = T // P
+    tok = lambda R: (R // cl) + P * (R % cl)   # noqa: E731
+    q_last = max(tok(R) for R in range(q_row0, q_row0 + q_rows))
+    k_first = min(tok(R) for R in range(k_row0, k_row0 + k_rows))
+    return k_first <= q_last
 
 
 @pytest.mark.parametrize("B,H,T,P,part,causal,sms", CASES)
@@ -49,10 +67,12 @@ def test_pair_schedule(B, H, T, P, part, causal, sms):
     assert sorted(tuple(int(x) for x in d) for d in dealt) == expect
 
     # key tiles of each item's walk, by brute force over all key tiles
+    seen = {}
     for b, h, r0, n0, r1, n1, nk, _ in items:
-        last = (r1 + n1 - 1) if n1 > 0 else (r0 + n0 - 1)   # global position of the pair's last query
-        brute = sum(1 for k0, _ in tiles if not causal or k0 <= last)
-        assert nk == brute
+        span = (r0, (r1 + n1 - r0) if n1 > 0 else n0)   # the pair's rows
+        if span not in seen:
+            seen[span] = sum(1 for k0, kn in tiles if not causal or tile_visible(T, P, part, *span, k0, kn))
+        assert nk == seen[span]
 
     # heaviest first: within the grouped phase the key counts of one head never grow;
     # the last phase holds the lightest items of the launch, heaviest first

@@ -46,12 +46,14 @@ def parse():
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
     ap.add_argument("--partition", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="override the workload's partition of the P ranks")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the workload's head count (smaller cases for counter captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-full", action="store_true",
                     help="time the oracle over the whole workload instead of a sample (small workloads)")
-    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses", "decode", "merge"],
+    ap.add_argument("--variant", default="ring", choices=["ring", "ulysses", "decode", "merge", "rope"],
                     help="ulysses: time ulysses_attn_fwd over P head-partitioned ranks (not the default line)")
     ap.add_argument("--direction", default="forward", choices=["forward", "backward"],
                     help="backward: time ring_attn_bwd instead (not the default bench line)")
@@ -398,11 +400,14 @@ def native_arm(args, w, rank, world, local_rank):
         qd, kd, vd = torch.empty_like(inp.q), torch.empty_like(inp.k), torch.empty_like(inp.v)
         ws_e = ba.ring_attn_fwd_workspace_size(w.B, w.H, w.T, w.d, inp.q.dtype, w.P, w.partition, args.mode,
                                                inp.kpm is not None or inp.am is not None, rope)
-        wse = torch.empty(max(ws_e, 1), dtype=torch.uint8, device=dev)
+        # two compute streams, each with its own workspace: the next group's launch
+        # fills the SMs as the current group's last work items drain
+        wse = [torch.empty(max(ws_e, 1), dtype=torch.uint8, device=dev) for _ in range(2)]
 
-        # Independent groups of heads (B == 1) or batch items are pipelined over three
+        # Independent groups of heads (B == 1) or batch items are pipelined over four
         # streams: host->device copy of group g+1 and device->host copy of group g-1
-        # run while group g computes, each group one ring_attn_fwd call.
+        # run while group g computes, each group one ring_attn_fwd call, the groups
+        # alternating between two compute streams.
         n_groups = 8
         if w.B == 1 and w.H % n_groups == 0:
             sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
@@ -411,6 +416,7 @@ def native_arm(args, w, rank, world, local_rank):
         else:
             n_groups, sl = 1, [(slice(None),)]
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_comp = [stream, torch.cuda.Stream(dev)]
         ev_in = [torch.cuda.Event() for _ in range(n_groups)]
         ev_comp = [torch.cuda.Event() for _ in range(n_groups)]
         ev_out = [torch.cuda.Event() for _ in range(n_groups)]
@@ -426,14 +432,15 @@ def native_arm(args, w, rank, world, local_rank):
                     kd[ix].copy_(kh[ix], non_blocking=True)
                     vd[ix].copy_(vh[ix], non_blocking=True)
                     ev_in[i].record(s_in)
-                stream.wait_event(ev_in[i])
+                cs = s_comp[i % 2]
+                cs.wait_event(ev_in[i])
                 if started[0]:
-                    stream.wait_event(ev_out[i])         # previous step's copy-out read these outputs
+                    cs.wait_event(ev_out[i])             # previous step's copy-out read these outputs
                 ba.ring_attn_fwd(qd[ix], kd[ix], vd[ix], P=w.P, partition=w.partition, mode=args.mode,
                                  key_padding_mask=kpm_i, attn_mask=inp.am, causal=w.causal, rope=rope,
-                                 rope_base=w.rope_base or 10000.0, out=out[ix], lse=lse[ix], workspace=wse,
-                                 stream=stream)
-                ev_comp[i].record(stream)
+                                 rope_base=w.rope_base or 10000.0, out=out[ix], lse=lse[ix], workspace=wse[i % 2],
+                                 stream=cs)
+                ev_comp[i].record(cs)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_comp[i])
                     oh[ix].copy_(out[ix], non_blocking=True)
@@ -449,8 +456,8 @@ def native_arm(args, w, rank, world, local_rank):
         a.record(s_in)            # the first operation of a step is a copy on s_in
         for _ in range(args.steps):
             e2e_step()
-        stream.wait_event(ev_out[-1])
-        s_out.wait_stream(stream)
+        for cs in s_comp:
+            s_out.wait_stream(cs)
         b.record(s_out)           # the last copy-out of the last step
         torch.cuda.synchronize()
         barrier()
@@ -737,6 +744,61 @@ def merge_arm(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def rope_arm(args, w, rank, world, local_rank):
+    """Time rope_apply on the workload's Q and K (one launch for both), bf16 in
+    and out.  Bound by HBM: 2 bytes read and 2 written per element and tensor."""
+    import blockwise_attention_gb300 as ba
+    from blockwise_attention_gb300.workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ba.load()
+    inp = make_inputs(w, dev)
+    qr, kr = torch.empty_like(inp.q), torch.empty_like(inp.k)
+    base = w.rope_base or 10000.0
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ba.rope_apply(inp.q, x2=inp.k, base=base, out=qr, out2=kr)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world, dev)
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    nbytes = 2.0 * inp.q.numel() * inp.q.element_size() * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {"metric": "RoPE of Q and K: HBM GB/s (read + write of both tensors)",
+            "value": world * gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"rope_of_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d": w.d, "base": base,
+                       "bytes_per_step": nbytes,
+                       "l2": f"Q and K ({nbytes / 2e9:.2f} GB) larger than the 129 MB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "rope_bf16_kernel",
+                         "algorithmic_bytes": nbytes, "kernel_ms": ms, "peak_source": f"{src} hbm_gbs (copy)"},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def decode_arm(args, rank, world, local_rank):
     """Time attn_decode_fwd on the decode workload (one query token per sequence,
     B=8, H=32, d=128, bf16, 64K-slot cache with ragged lengths).  Bound by HBM:
@@ -805,6 +867,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.partition:
         w = w.replace(partition=args.partition)
+    if args.heads:
+        w = w.replace(H=args.heads, name=f"{w.name}_h{args.heads}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -822,6 +886,8 @@ def main():
             decode_arm(args, rank, world, local_rank)
         elif args.variant == "merge":
             merge_arm(args, w, rank, world, local_rank)
+        elif args.variant == "rope":
+            rope_arm(args, w, rank, world, local_rank)
         else:
             native_arm(args, w, rank, world, local_rank)
     finally:

@@ -177,47 +177,82 @@ __global__ void tile_class_kernel(const Geom g, int8_t *cls) {
         (int8_t)(!any ? BA_TILE_EMPTY : (all ? BA_TILE_FULL : BA_TILE_PARTIAL));
 }
 
-// a <- merge(a, b): one warp per row.
+// LSE merge weights (natural log) of one row: a <- wa a + wb b, lse <- L.
+// Returns false when b carries no keys and a stays as it is.
+__device__ __forceinline__ bool merge_row_weights(float A, float Bv, float &wa, float &wb, float &L) {
+    if (Bv == -INFINITY) {
+        if (A != -INFINITY) return false;   // nothing to fold in: a unchanged
+        wa = wb = 0.f;                      // neither side saw a key: out = 0, lse = -inf
+        L = -INFINITY;
+        return true;
+    }
+    if (A == -INFINITY) {
+        wa = 0.f;
+        wb = 1.f;
+        L = Bv;
+        return true;
+    }
+    const float M = fmaxf(A, Bv);
+    L = M + logf(expf(A - M) + expf(Bv - M));
+    wa = expf(A - L);
+    wb = expf(Bv - L);
+    return true;
+}
+
+// a <- merge(a, b) for rows of d <= 128 columns, d a multiple of 4 and 16-byte
+// aligned rows: one warp per row, lane c holding columns 4c .. 4c+3; each warp
+// takes two rows per iteration and issues all four loads of both (LSEs and
+// rows) before it computes, so that the loads of a row do not wait for its
+// weights.  Streaming loads and stores: every byte is touched once.
+__global__ void __launch_bounds__(256) merge_vec_kernel(float4 *__restrict__ oa, float *__restrict__ la,
+                                                        const float4 *__restrict__ ob,
+                                                        const float *__restrict__ lb, long long rows, int nv) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const long long w0 = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const bool col = lane < nv;
+    for (long long r0 = w0; r0 < rows; r0 += 2 * warps) {
+        const long long rr[2] = {r0, r0 + warps};
+        float A[2], Bv[2];
+        float4 x[2], y[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const bool in = rr[u] < rows;
+            A[u] = in ? __ldcs(la + rr[u]) : 0.f;
+            Bv[u] = in ? __ldcs(lb + rr[u]) : 0.f;
+            x[u] = in && col ? __ldcs(oa + rr[u] * nv + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+            y[u] = in && col ? __ldcs(ob + rr[u] * nv + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (rr[u] >= rows) continue;
+            float wa, wb, L;
+            if (!merge_row_weights(A[u], Bv[u], wa, wb, L)) continue;
+            if (col) {
+                float4 o;
+                // a side of weight 0 contributes 0 whatever its row holds
+                o.x = (wa != 0.f ? wa * x[u].x : 0.f) + wb * y[u].x;
+                o.y = (wa != 0.f ? wa * x[u].y : 0.f) + wb * y[u].y;
+                o.z = (wa != 0.f ? wa * x[u].z : 0.f) + wb * y[u].z;
+                o.w = (wa != 0.f ? wa * x[u].w : 0.f) + wb * y[u].w;
+                __stcs(oa + rr[u] * nv + lane, o);
+            }
+            if (lane == 0) la[rr[u]] = L;
+        }
+    }
+}
+
+// a <- merge(a, b), any d: one warp per row.
 __global__ void merge_kernel(float *__restrict__ oa, float *__restrict__ la, const float *__restrict__ ob,
                              const float *__restrict__ lb, long long rows, int d) {
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-        const float A = la[r], Bv = lb[r];
         float wa, wb, L;
-        if (Bv == -INFINITY && A != -INFINITY) {
-            continue;   // nothing to fold in: a unchanged
-        } else if (Bv == -INFINITY) {
-            wa = 0.f;   // neither side saw a key: out = 0, lse = -inf
-            wb = 0.f;
-            L = -INFINITY;
-        } else if (A == -INFINITY) {
-            wa = 0.f;
-            wb = 1.f;
-            L = Bv;
-        } else {
-            const float M = fmaxf(A, Bv);
-            L = M + logf(expf(A - M) + expf(Bv - M));
-            wa = expf(A - L);
-            wb = expf(Bv - L);
-        }
+        if (!merge_row_weights(la[r], lb[r], wa, wb, L)) continue;
         float *pa = oa + r * d;
         const float *pb = ob + r * d;
-        if ((d & 3) == 0) {
-            float4 *va = reinterpret_cast<float4 *>(pa);
-            const float4 *vb = reinterpret_cast<const float4 *>(pb);
-            for (int c = lane; c < d / 4; c += 32) {
-                const float4 y = vb[c];
-                float4 x = wa != 0.f ? va[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-                x.x = wa * x.x + wb * y.x;
-                x.y = wa * x.y + wb * y.y;
-                x.z = wa * x.z + wb * y.z;
-                x.w = wa * x.w + wb * y.w;
-                va[c] = x;
-            }
-        } else {
-            for (int c = lane; c < d; c += 32) pa[c] = (wa != 0.f ? wa * pa[c] : 0.f) + wb * pb[c];
-        }
+        for (int c = lane; c < d; c += 32) pa[c] = (wa != 0.f ? wa * pa[c] : 0.f) + wb * pb[c];
         if (lane == 0) la[r] = L;
     }
 }
@@ -236,6 +271,7 @@ struct RopeArgs {
     const int32_t *positions;
     double pos_scale;       // Position Interpolation: angle = (position * pos_scale) * theta
     Thetas th;
+    double tab_cos[64], tab_sin[64];   // cos, sin (n pi / 32), n = 0 .. 63 (sincos_table)
 };
 
 // fp64 -> bf16 with one rounding (ties to even): truncate to fp32, make the
@@ -300,62 +336,165 @@ __device__ __forceinline__ uint16_t rot_bf16(float x0, const Split4 &a, float x1
     return (uint16_t)bits;
 }
 
-// bfloat16, 8 elements (4 pairs) per thread per head: one thread per
-// (position t, 4 consecutive pairs); the angles' cos/sin are computed once in
-// fp64 and applied to those pairs in every tensor and (b, h).
+// sin and cos of an fp64 angle a, table-driven (Tang's method): a = n pi/32 + r
+// with |r| <= pi/64, r by a three-part Cody-Waite reduction (pi/32 split into
+// pieces of 27, 27 and 53 significant bits, so that n * piece is exact for
+// |n| < 2^26); sin r, cos r by their Taylor series (terms through r^9 / 9! and
+// r^8 / 8!: the next terms are below 2^-64 for |r| <= pi/64); then the angle
+// sum with the table entries cos, sin (n pi / 32), n mod 64.  Absolute error of
+// a few units of 2^-53.  Angles of 2^20 and beyond take sincos().
+__device__ __forceinline__ void sincos_table(double a, const double2 *tab, double &sn, double &cs) {
+    constexpr double K = 0x1.45f306dc9c883p+3;        // 32 / pi
+    constexpr double P1 = 0x1.921fb54000000p-4;       // pi / 32 = P1 + P2 + P3 (+ 2^-118)
+    constexpr double P2 = 0x1.10b4612000000p-34;
+    constexpr double P3 = -0x1.676733ae8fe48p-64;
+    if (!(fabs(a) < 1048576.0)) {
+        sincos(a, &sn, &cs);
+        return;
+    }
+    const double n = rint(a * K);
+    double r = fma(-n, P1, a);
+    r = fma(-n, P2, r);
+    r = fma(-n, P3, r);
+    const double z = r * r;
+    // sin r = r - r^3/3! + r^5/5! - r^7/7! + r^9/9!;  cos r = 1 - r^2/2! + ... + r^8/8!
+    const double sp = fma(z, fma(z, fma(z, 1.0 / 362880.0, -1.0 / 5040.0), 1.0 / 120.0), -1.0 / 6.0);
+    const double sr = fma(r * z, sp, r);
+    const double cp = fma(z, fma(z, fma(z, 1.0 / 40320.0, -1.0 / 720.0), 1.0 / 24.0), -0.5);
+    const double cr = fma(z, cp, 1.0);
+    const double2 t = tab[(int)((long long)n & 63)];   // (cos, sin) of (n mod 64) pi / 32
+    cs = fma(t.x, cr, -t.y * sr);
+    sn = fma(t.y, cr, t.x * sr);
+}
+
+// c = hi + lo with hi of 16 significant bits (its product with a bfloat16 is
+// exact in fp32) and lo the fp32 rounding of the rest (|lo| < 2^-15 |c|).
+__device__ __forceinline__ void split_hi_lo(double c, float &hi, float &lo) {
+    hi = __uint_as_float(__float_as_uint(__double2float_rn(c)) & 0xFFFFFF00u);
+    lo = __double2float_rn(c - (double)hi);
+}
+
+// Fast rounding of y = p + t (a rotated coordinate, computed in fp32 with
+// error at most err) to bfloat16: true when no bfloat16 rounding midpoint lies
+// within err of y, so that round(y) is the rounding of the exact value (Ziv's
+// rounding test).  The midpoint of y's bfloat16 interval is the only candidate
+// while err < 2^-10 |y|; |y - mid| is exact (same binade).
+__device__ __forceinline__ bool rounding_safe(float y, float err) {
+    const float mid = __uint_as_float((__float_as_uint(y) & 0xFFFF0000u) | 0x8000u);
+    return err <= fabsf(y) * 0x1p-10f && fabsf(y - mid) > err;
+}
+
+struct RopeRowPair {
+    float ch, cl, sh, sl;   // split cos and sin of the pair's angle
+};
+
+// One output pair (y0, y1) = (x0 c - x1 s, x0 s + x1 c) of bfloat16 inputs by
+// the fast path; ok is false when either coordinate fails the rounding test.
+__device__ __forceinline__ void rot_fast(float x0, float x1, const RopeRowPair &k, uint16_t &o0, uint16_t &o1,
+                                         bool &ok) {
+    const float ax = fabsf(x0) + fabsf(x1);
+    const float h0 = fmaf(x0, k.ch, -(x1 * k.sh));         // exact products, one rounding
+    const float y0 = h0 + fmaf(x0, k.cl, -(x1 * k.sl));
+    const float h1 = fmaf(x0, k.sh, x1 * k.ch);
+    const float y1 = h1 + fmaf(x0, k.sl, x1 * k.cl);
+    // error bound: 2^-24 for each of the two roundings of the sum, 2^-38 |x|
+    // for the split of c, s and the low products; doubled
+    const float e0 = fmaf(0x1p-23f, fabsf(h0) + fabsf(y0), 0x1p-37f * ax);
+    const float e1 = fmaf(0x1p-23f, fabsf(h1) + fabsf(y1), 0x1p-37f * ax);
+    ok = rounding_safe(y0, e0) && rounding_safe(y1, e1);
+    o0 = __bfloat16_as_ushort(__float2bfloat16_rn(y0));
+    o1 = __bfloat16_as_ushort(__float2bfloat16_rn(y1));
+}
+
+// bfloat16 with d a multiple of 8.  A CTA of 256 threads covers TP = 2048 / d
+// positions x d columns; thread (t, g) owns the four pairs 4g .. 4g+3 at
+// position t.  It computes their angles' cos and sin once (fp64, table-driven)
+// and rotates those pairs in every row of the CTA's share of the (tensor, b, h)
+// rows, four rows' 16-byte loads in flight at a time.  The rotation runs in
+// fp32 with a rounding test; the rare coordinate the test cannot decide is
+// recomputed exactly (rot_bf16), so every output is the exact rotation rounded
+// once to bfloat16.
 template <bool VEC>
-__global__ void rope_bf16_kernel(const RopeArgs a) {
-    const int groups = a.d / 8;
-    const long long n = (long long)a.T * groups;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(e / groups), c0 = (int)(e % groups) * 4;
-        const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
-        Split4 cs[4], sn[4], ncs[4];
+__global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
+    __shared__ double2 tab[64];
+    __shared__ double2 exact[4][256];   // fp64 (cos, sin) of each thread's pairs, for the exact path
+    if (threadIdx.x < 64) tab[threadIdx.x] = make_double2(a.tab_cos[threadIdx.x], a.tab_sin[threadIdx.x]);
+    __syncthreads();
+    const int G = a.d / 8;
+    const int TP = 256 / G;
+    const int tl = threadIdx.x / G, grp = threadIdx.x % G;
+    const long long t = (long long)blockIdx.x * TP + tl;
+    if (tl >= TP || t >= a.T) return;
+    const int c0 = grp * 4;
+    const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
+    RopeRowPair k[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            double sv, cv;
-            sincos(m * a.th.th[c0 + i], &sv, &cv);
-            cs[i] = split16(cv);
-            sn[i] = split16(sv);
+    for (int i = 0; i < 4; ++i) {
+        double cs, sn;
+        sincos_table(m * a.th.th[c0 + i], tab, sn, cs);
+        split_hi_lo(cs, k[i].ch, k[i].cl);
+        split_hi_lo(sn, k[i].sh, k[i].sl);
+        exact[i][threadIdx.x] = make_double2(cs, sn);
+    }
+    const int rows = a.n * a.B * a.H;
+    const int per = (rows + gridDim.y - 1) / gridDim.y;
+    const int r_begin = blockIdx.y * per;
+    const int r_end = r_begin + per < rows ? r_begin + per : rows;
+    constexpr int U = 4;
+    for (int r0 = r_begin; r0 < r_end; r0 += U) {
+        uint32_t w[U][4];
+        __nv_bfloat16 *py[U];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) ncs[i].k[k] = -cs[i].k[k];
+        for (int u = 0; u < U; ++u) {
+            const int r = r0 + u;
+            py[u] = nullptr;
+            if (r >= r_end) continue;
+            const int ti = r / (a.B * a.H), bh = r % (a.B * a.H), b = bh / a.H, h = bh % a.H;
+            const __nv_bfloat16 *px = static_cast<const __nv_bfloat16 *>(a.x[ti]) + b * a.sB[ti] +
+                                      h * a.sH[ti] + t * a.sT[ti] + 2 * c0;
+            py[u] = static_cast<__nv_bfloat16 *>(a.y[ti]) + ((long long)bh * a.T + t) * a.d + 2 * c0;
+            if (VEC) {
+                const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(px));
+                w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[u][i] = (uint32_t)__bfloat16_as_ushort(px[2 * i]) |
+                              ((uint32_t)__bfloat16_as_ushort(px[2 * i + 1]) << 16);
+            }
         }
-        for (int ti = 0; ti < a.n; ++ti) {
-            const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(a.x[ti]);
-            __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(a.y[ti]);
-            for (int b = 0; b < a.B; ++b) {
-                for (int h = 0; h < a.H; ++h) {
-                    const __nv_bfloat16 *px = xb + b * a.sB[ti] + h * a.sH[ti] + (long long)t * a.sT[ti] + 2 * c0;
-                    uint16_t in[8], out[8];
-                    if (VEC) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(px);
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            in[2 * i] = (uint16_t)(w[i] & 0xFFFFu);
-                            in[2 * i + 1] = (uint16_t)(w[i] >> 16);
-                        }
-                    } else {
+        for (int u = 0; u < U; ++u) {
+            if (py[u] == nullptr) continue;
+            uint16_t out[8];
+            bool ok[4];
+            float x0[4], x1[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) in[i] = __bfloat16_as_ushort(px[i]);
-                    }
+            for (int i = 0; i < 4; ++i) {
+                x0[i] = __uint_as_float(w[u][i] << 16);
+                x1[i] = __uint_as_float(w[u][i] & 0xFFFF0000u);
+                rot_fast(x0[i], x1[i], k[i], out[2 * i], out[2 * i + 1], ok[i]);
+            }
+            const bool all_ok = ok[0] && ok[1] && ok[2] && ok[3];
+            if (!all_ok) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float x0 = __uint_as_float((uint32_t)in[2 * i] << 16);
-                        const float x1 = __uint_as_float((uint32_t)in[2 * i + 1] << 16);
-                        out[2 * i] = rot_bf16(x0, cs[i], x1, sn[i]);        // x0 cos - x1 sin
-                        out[2 * i + 1] = rot_bf16(x0, sn[i], x1, ncs[i]);   // x0 sin - x1 (-cos)
-                    }
-                    __nv_bfloat16 *py = yb + (((long long)b * a.H + h) * a.T + t) * a.d + 2 * c0;
-                    uint4 o;
-                    o.x = out[0] | ((uint32_t)out[1] << 16);
-                    o.y = out[2] | ((uint32_t)out[3] << 16);
-                    o.z = out[4] | ((uint32_t)out[5] << 16);
-                    o.w = out[6] | ((uint32_t)out[7] << 16);
-                    *reinterpret_cast<uint4 *>(py) = o;
+                for (int i = 0; i < 4; ++i) {
+                    if (ok[i]) continue;
+                    const double2 e = exact[i][threadIdx.x];
+                    const Split4 c4 = split16(e.x), s4 = split16(e.y);
+                    Split4 nc4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) nc4.k[j] = -c4.k[j];
+                    out[2 * i] = rot_bf16(x0[i], c4, x1[i], s4);        // x0 cos - x1 sin
+                    out[2 * i + 1] = rot_bf16(x0[i], s4, x1[i], nc4);   // x0 sin - x1 (-cos)
                 }
             }
+            uint4 o;
+            o.x = out[0] | ((uint32_t)out[1] << 16);
+            o.y = out[2] | ((uint32_t)out[3] << 16);
+            o.z = out[4] | ((uint32_t)out[5] << 16);
+            o.w = out[6] | ((uint32_t)out[7] << 16);
+            *reinterpret_cast<uint4 *>(py[u]) = o;
         }
     }
 }
@@ -495,17 +634,48 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
     a.pos_scale = pos_scale > 0.f ? (double)pos_scale : 1.0;   // a float times an int32 is exact in fp64
     if ((long long)T * d == 0 || B == 0 || H == 0) return BA_OK;
     const int threads = 256;
-    const long long per = dtype == BA_BF16 && d % 8 == 0 ? d / 8 : d / 2;
+    if (dtype == BA_BF16 && d % 8 == 0) {
+        // the table of sincos_table: cos, sin (n pi / 32), from the first octant by symmetry
+        const long double pi = 3.14159265358979323846264338327950288L;
+        for (int n = 0; n < 64; ++n) {
+            const int q = n / 16, m = n % 16;   // angle = q pi/2 + m pi/32
+            long double c = cosl(pi * m / 32), sv = sinl(pi * m / 32);
+            if (m == 0) {
+                c = 1;
+                sv = 0;
+            }
+            for (int i = 0; i < q; ++i) {   // rotate by pi/2: (c, s) -> (-s, c)
+                const long double t = c;
+                c = -sv;
+                sv = t;
+            }
+            a.tab_cos[n] = (double)c;
+            a.tab_sin[n] = (double)sv;
+        }
+        const int per_cta = 2048 / d;                       // positions per CTA
+        const long long gx = ((long long)T + per_cta - 1) / per_cta;
+        const long long rows = (long long)a.n * B * H;
+        const int dev = current_device();
+        const long long want = 8LL * (dev >= 0 && g_num_sms[dev] > 0 ? g_num_sms[dev] : 152);
+        long long gy = (want + gx - 1) / gx;                // split the rows when positions are few
+        if (gy > rows) gy = rows;
+        if (gy > 65535) gy = 65535;
+        if (gy < 1) gy = 1;
+        if (gx > 0x7fffffffLL) return BA_ERR_SHAPE;
+        const dim3 grid((unsigned)gx, (unsigned)gy);
+        if (vec)
+            rope_bf16_kernel<true><<<grid, threads, 0, s>>>(a);
+        else
+            rope_bf16_kernel<false><<<grid, threads, 0, s>>>(a);
+        return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+    }
+    const long long per = d / 2;
     long long blocks = ((long long)T * per + threads - 1) / threads;
     if (blocks > 1 << 20) blocks = 1 << 20;
     if (dtype == BA_F32)
         rope_f32_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
-    else if (d % 8 != 0)
-        rope_bf16_pair_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
-    else if (vec)
-        rope_bf16_kernel<true><<<(unsigned)blocks, threads, 0, s>>>(a);
     else
-        rope_bf16_kernel<false><<<(unsigned)blocks, threads, 0, s>>>(a);
+        rope_bf16_pair_kernel<<<(unsigned)blocks, threads, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -667,9 +837,16 @@ int attn_merge(float *out_a, float *lse_a, const float *out_b, const float *lse_
     int rc = device_setup(dev);
     if (rc) return rc;
     long long blocks = (rows + 7) / 8;
-    const long long cap = (long long)g_num_sms[dev] * 16;
+    const long long cap = (long long)g_num_sms[dev] * 8;   // eight resident 256-thread CTAs per SM
     if (blocks > cap) blocks = cap;
-    merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out_a, lse_a, out_b, lse_b, rows, d);
+    const bool vec = (d & 3) == 0 && d <= 128 && (reinterpret_cast<uintptr_t>(out_a) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(out_b) & 15) == 0;
+    if (vec)
+        merge_vec_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<float4 *>(out_a), lse_a,
+                                                                reinterpret_cast<const float4 *>(out_b), lse_b,
+                                                                rows, d / 4);
+    else
+        merge_kernel<<<(unsigned)blocks, 256, 0, stream>>>(out_a, lse_a, out_b, lse_b, rows, d);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 

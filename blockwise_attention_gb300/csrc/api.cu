@@ -159,7 +159,7 @@ int heads_per_group(int B, int H, long long keys, int d, int dtype) {
 // pair, one thread per query row.
 __global__ void tile_class_kernel(const Geom g, int8_t *cls) {
     const int kg = blockIdx.x, qg = blockIdx.y, b = blockIdx.z;
-    const QTile q = q_tile(g, qg, b, 0);
+    const QTile q = q_tile<false>(g, qg, b, 0);   // masks: never striped
     const KTile k = k_tile_by_id(g, kg);
     const int i = threadIdx.x;
     int any = 0, all = 1;
@@ -756,7 +756,7 @@ int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int 
     g.tail_levels = pair_tail_levels(g, num_sms);
     const int heavy_items = (n_pairs(g) - g.tail_levels) * B * H;
     for (long long w = 0; items && w < n && w < capacity; ++w) {
-        const QPair p = work_pair(g, (int)w);
+        const QPair p = g.striped ? work_pair<true>(g, (int)w) : work_pair<false>(g, (int)w);
         int32_t *o = items + 8 * w;
         o[0] = p.q0.b;
         o[1] = p.q0.h;
@@ -764,7 +764,7 @@ int ba_pair_schedule(int B, int H, int T, int P, int partition, int causal, int 
         o[3] = p.q0.len;
         o[4] = p.q1.row0;
         o[5] = p.q1.len;
-        o[6] = pair_count(g, p);
+        o[6] = g.striped ? pair_count<true>(g, p) : pair_count<false>(g, p);
         o[7] = w < heavy_items ? 0 : 1;
     }
     return (int)n;

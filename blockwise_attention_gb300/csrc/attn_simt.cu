@@ -24,12 +24,12 @@ __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-template <int D, typename Tin>
+template <int D, typename Tin, bool S>
 __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
     __shared__ float Ks[SUB][D + 1];
     __shared__ float Vs[SUB][D];
     const Geom &g = a.g;
-    const QTile qt = work_item(g, blockIdx.x);
+    const QTile qt = work_item<S>(g, blockIdx.x);
     const int r = threadIdx.x;
     const bool valid = r < qt.len;
     const long long qpos = qt.pos0 + r;
@@ -40,21 +40,21 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
     float q[D], o[D];
 #pragma unroll
     for (int c = 0; c < D; ++c) {
-        q[c] = valid ? to_f32(qb[row_token(g, qt.row0 + r) * a.qsT + c]) : 0.f;
+        q[c] = valid ? to_f32(qb[row_token<S>(g, qt.row0 + r) * a.qsT + c]) : 0.f;
         o[c] = 0.f;
     }
     float m = -INFINITY, l = 0.f;   // running max (log2 units) and denominator
 
     KWalk wk;
-    kwalk_begin(g, qt, wk);
+    kwalk_begin<S>(g, qt, wk);
     KTile kt;
-    while (kwalk_next(g, qt, wk, kt)) {
+    while (kwalk_next<S>(g, qt, wk, kt)) {
         for (int s0 = 0; s0 < kt.len; s0 += SUB) {
             __syncthreads();
             for (int e = threadIdx.x; e < SUB * D; e += blockDim.x) {
                 int j = e / D, c = e % D;
                 bool in = s0 + j < kt.len;
-                long long row = g.ring ? row_token(g, kt.row0 + s0 + j) : kt.row0 + s0 + j;
+                const long long row = row_token<S>(g, kt.row0 + s0 + j);
                 Ks[j][c] = in ? to_f32(kb[row * a.ksT + c]) : 0.f;
                 Vs[j][c] = in ? to_f32(vb[row * a.vsT + c]) : 0.f;
             }
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
         }
     }
     if (!valid) return;
-    const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row(g, qt, r);
+    const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row<S>(g, qt, r);
     const float acc_l = a.acc_lse ? a.acc_lse[row_flat] : -INFINITY;
     const RowFinal f = row_final(m, l, acc_l);
 #pragma unroll
@@ -100,14 +100,19 @@ __global__ void __launch_bounds__(TILE) attn_simt_kernel(const AttnArgs a) {
     a.lse[row_flat] = f.lse;
 }
 
-template <int D>
-int launch_d(const AttnArgs &a, cudaStream_t s) {
+template <int D, bool S>
+int launch_ds(const AttnArgs &a, cudaStream_t s) {
     dim3 grid(a.g.n_items);
     if (a.dtype == BA_F32)
-        attn_simt_kernel<D, float><<<grid, TILE, 0, s>>>(a);
+        attn_simt_kernel<D, float, S><<<grid, TILE, 0, s>>>(a);
     else
-        attn_simt_kernel<D, __nv_bfloat16><<<grid, TILE, 0, s>>>(a);
+        attn_simt_kernel<D, __nv_bfloat16, S><<<grid, TILE, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+template <int D>
+int launch_d(const AttnArgs &a, cudaStream_t s) {
+    return a.g.striped ? launch_ds<D, true>(a, s) : launch_ds<D, false>(a, s);
 }
 
 }  // namespace

@@ -146,7 +146,7 @@ __device__ __noinline__ uint32_t keep_bits(const Geom &g, int b, long long qpos,
 // Kernel
 // ----------------------------------------------------------------------------
 
-template <int D>
+template <int D, bool S>
 __global__ void __launch_bounds__(320, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_arrive(bar(C::B_ITEMFULL + sl));
                     break;
                 }
-                const QPair p = work_pair(g, w);
+                const QPair p = work_pair<S>(g, w);
                 const bool has1 = p.q1.len > 0;
                 misc[4 + sl] = (uint32_t)w;
-                misc[2 + sl] = (uint32_t)pair_count(g, p) | (has1 ? 0x80000000u : 0u);
+                misc[2 + sl] = (uint32_t)pair_count<S>(g, p) | (has1 ? 0x80000000u : 0u);
                 mbar_arrive(bar(C::B_ITEMFULL + sl));
                 if (it_local > 0 && !mbar_wait(bar(C::B_QEMPTY), (it_local - 1) & 1, abort, a.err, lim)) {
                     ok = false;
@@ -254,19 +254,19 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 mbar_arrive_expect_tx(bar(C::B_QFULL), (has1 ? 2 : 1) * C::TILE_BYTES);
                 for (int bx = 0; bx < C::NBOX; ++bx)
-                    tma_load_rows(sQ + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q0.row0, p.q0.h, p.q0.b, bar(C::B_QFULL));
+                    tma_load_rows<S>(sQ + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q0.row0, p.q0.h, p.q0.b, bar(C::B_QFULL));
                 if (has1)
                     for (int bx = 0; bx < C::NBOX; ++bx)
-                        tma_load_rows(sQ + C::TILE_BYTES + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q1.row0, p.q0.h,
+                        tma_load_rows<S>(sQ + C::TILE_BYTES + bx * C::BOX_BYTES, &tq, g, bx * 64, p.q1.row0, p.q0.h,
                                       p.q0.b, bar(C::B_QFULL));
                 ++qfills;
                 KWalk wk;
-                kwalk_begin(g, p.span, wk);
+                kwalk_begin<S>(g, p.span, wk);
                 KTile kt;
                 int c0, c1;
                 int prev_row = -1;   // k/v row of the tile whose V is still to be loaded
                 for (;;) {
-                    const bool more = pair_next(g, p, wk, kt, c0, c1);
+                    const bool more = pair_next<S>(g, p, wk, kt, c0, c1);
                     if (more) {
                         const uint32_t st = kfill % C::KS, use = kfill / C::KS;
                         if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_rows(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, g, bx * 64, kt.row0,
+                            tma_load_rows<S>(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, g, bx * 64, kt.row0,
                                           p.q0.h, p.q0.b, bar(C::B_KFULL + st));
                         ++kfill;
                     }
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
                         for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_rows(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, g, bx * 64, prev_row,
+                            tma_load_rows<S>(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, g, bx * 64, prev_row,
                                           p.q0.h, p.q0.b, bar(C::B_VFULL + st));
                         ++vfill;
                     }
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(320, 1)
                 tcnt += n_tiles;
                 continue;
             }
-            const QPair pr = work_pair(g, (int)item);
+            const QPair pr = work_pair<S>(g, (int)item);
             const QTile qt = x ? pr.q1 : pr.q0;
             const long long qpos = qt.pos0 + row;
             float m_ref = -INFINITY, l = 0.f;
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(320, 1)
             ++ox;
             tc_fence_after();
             const bool valid = row < qt.len;
-            const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row(g, qt, row);
+            const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row<S>(g, qt, row);
             const float acc_l = (a.acc_lse != nullptr && valid) ? a.acc_lse[row_flat] : -INFINITY;
             const RowFinal f = row_final(m_ref, n > 0 ? l : 0.f, acc_l);
 #pragma unroll
@@ -628,15 +628,15 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-template <int D>
+template <int D, bool S>
 int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
     using C = Cfg<D>;
     static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return BA_ERR_CUDA;
     int grid = a.g.n_items < num_sms ? a.g.n_items : num_sms;
-    attn_tc_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
+    attn_tc_kernel<D, S><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -652,8 +652,13 @@ int launch_attn_tc(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_
     ap.g.n_items = n_pairs(a.g) * a.g.B * a.g.H;
     ap.g.tail_levels = pair_tail_levels(a.g, num_sms);
     if (ap.g.n_items == 0 || a.g.n_qtiles == 0) return BA_OK;
-    if (a.g.d == 128) return launch_d<128>(ap, m, num_sms, s);
-    if (a.g.d == 64) return launch_d<64>(ap, m, num_sms, s);
+    if (a.g.striped) {
+        if (a.g.d == 128) return launch_d<128, true>(ap, m, num_sms, s);
+        if (a.g.d == 64) return launch_d<64, true>(ap, m, num_sms, s);
+        return BA_ERR_SHAPE;
+    }
+    if (a.g.d == 128) return launch_d<128, false>(ap, m, num_sms, s);
+    if (a.g.d == 64) return launch_d<64, false>(ap, m, num_sms, s);
     return BA_ERR_SHAPE;
 }
 

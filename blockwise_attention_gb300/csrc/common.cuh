@@ -43,6 +43,10 @@ constexpr float LN2 = 0.6931471805599453f;
 // (rank, step) pair is the lower triangle with its diagonal (c <= r) or
 // without it (c > r), and "key position <= query position" holds as in the
 // other partitions.  Masks are indexed by token and are not taken here.
+//
+// The geometry functions below take the striped choice as a template
+// parameter S (instantiated from g.striped by the launching code), so that the
+// kernels of the other partitions compile without it.
 struct Geom {
     int B, H, d;
     int ring;
@@ -90,6 +94,7 @@ __host__ __device__ inline int chunk_owner(const Geom &g, int c) {
 }
 
 // Query tile with id qg (0 .. n_qtiles-1) of head (b, h).
+template <bool S>
 __host__ __device__ inline QTile q_tile(const Geom &g, int qg, int b, int h) {
     QTile t;
     t.g = qg;
@@ -100,7 +105,7 @@ __host__ __device__ inline QTile q_tile(const Geom &g, int qg, int b, int h) {
         t.row0 = c * g.CL + i * TILE;
         int end = (c + 1) * g.CL;
         t.len = (t.row0 + TILE < end ? t.row0 + TILE : end) - t.row0;
-        t.pos0 = g.striped ? i * TILE : t.row0;   // striped: local index within the rank
+        t.pos0 = S ? i * TILE : t.row0;   // striped: local index within the rank
         t.rank = chunk_owner(g, c);
     } else {
         t.row0 = qg * TILE;
@@ -152,17 +157,20 @@ struct KWalk {
 // Position of the first key of chunk c for a query tile of rank qrank: its
 // global position, or in the striped ring its local index 0 shifted by one
 // when the key's rank follows the query's (see Geom).
+template <bool S>
 __host__ __device__ __forceinline__ int chunk_pos0(const Geom &g, int c, int qrank) {
-    return g.striped ? (c > qrank ? 1 : 0) : c * g.CL;
+    return S ? (c > qrank ? 1 : 0) : c * g.CL;
 }
 
+template <bool S>
 __host__ __device__ __forceinline__ void kwalk_set_chunk(const Geom &g, KWalk &w, int c) {
     w.row = c * g.CL;
     w.chunk_end = w.row + g.CL;
     w.idx = c * g.nkt_pc;
-    w.pos_off = chunk_pos0(g, c, w.qrank) - w.row;
+    w.pos_off = chunk_pos0<S>(g, c, w.qrank) - w.row;
 }
 
+template <bool S>
 __host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile &q, KWalk &w) {
     w.q_first = (int)q.pos0;
     w.q_last = (int)q.pos0 + q.len - 1;
@@ -173,7 +181,7 @@ __host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile 
         w.s = g.s_begin;
         w.src = ((q.rank - w.s) % g.P + g.P) % g.P;
         if (w.s < g.s_end) {
-            kwalk_set_chunk(g, w, w.src);
+            kwalk_set_chunk<S>(g, w, w.src);
         } else {
             w.row = w.chunk_end = 0;   // empty step range: the walk is over
             w.ci = 1;
@@ -190,25 +198,27 @@ __host__ __device__ __forceinline__ void kwalk_begin(const Geom &g, const QTile 
 }
 
 // Moves to the next chunk of the walk; false when the walk is over.
+template <bool S>
 __host__ __device__ __forceinline__ bool kwalk_next_chunk(const Geom &g, KWalk &w) {
     if (!g.ring) return false;
     if (g.zigzag && w.ci == 0) {
         w.ci = 1;
-        kwalk_set_chunk(g, w, 2 * g.P - 1 - w.src);
+        kwalk_set_chunk<S>(g, w, 2 * g.P - 1 - w.src);
         return true;
     }
     w.ci = 0;
     if (++w.s >= g.s_end) return false;
     w.src = w.src == 0 ? g.P - 1 : w.src - 1;
-    kwalk_set_chunk(g, w, w.src);
+    kwalk_set_chunk<S>(g, w, w.src);
     return true;
 }
 
 // Next non-EMPTY key tile of the walk into k; false at the end.
+template <bool S>
 __host__ __device__ __forceinline__ bool kwalk_next(const Geom &g, const QTile &q, KWalk &w, KTile &k) {
     for (;;) {
         if (w.row >= w.chunk_end) {
-            if (!kwalk_next_chunk(g, w)) return false;
+            if (!kwalk_next_chunk<S>(g, w)) return false;
             continue;
         }
         const int row = w.row;
@@ -243,13 +253,14 @@ __host__ __device__ __forceinline__ bool kwalk_next(const Geom &g, const QTile &
 // this is a sum over the walk's chunks (a chunk contributes its tiles that start
 // at or before q's last row under causal masking, all of them otherwise), so it
 // costs a few operations per chunk instead of a walk over every tile.
+template <bool S>
 __host__ __device__ inline int kwalk_count(const Geom &g, const QTile &q) {
     if (g.cls) {
         KWalk w;
-        kwalk_begin(g, q, w);
+        kwalk_begin<S>(g, q, w);
         KTile k;
         int n = 0;
-        while (kwalk_next(g, q, w, k)) ++n;
+        while (kwalk_next<S>(g, q, w, k)) ++n;
         return n;
     }
     const long long q_last = q.pos0 + q.len - 1;
@@ -264,8 +275,8 @@ __host__ __device__ inline int kwalk_count(const Geom &g, const QTile &q) {
     int n = 0;
     int src = ((q.rank - g.s_begin) % g.P + g.P) % g.P;
     for (int s = g.s_begin; s < g.s_end; ++s) {
-        n += chunk_tiles(chunk_pos0(g, src, q.rank), g.CL);
-        if (g.zigzag) n += chunk_tiles(chunk_pos0(g, 2 * g.P - 1 - src, q.rank), g.CL);
+        n += chunk_tiles(chunk_pos0<S>(g, src, q.rank), g.CL);
+        if (g.zigzag) n += chunk_tiles(chunk_pos0<S>(g, 2 * g.P - 1 - src, q.rank), g.CL);
         src = src == 0 ? g.P - 1 : src - 1;
     }
     return n;
@@ -273,20 +284,23 @@ __host__ __device__ inline int kwalk_count(const Geom &g, const QTile &q) {
 
 // Token of row R of a ring tensor: R itself, or r + P u for row R = r CL + u
 // of the striped ring.
+template <bool S>
 __host__ __device__ __forceinline__ long long row_token(const Geom &g, long long R) {
-    if (!g.striped) return R;
+    if (!S) return R;
     const long long r = R / g.CL;
     return r + (long long)g.P * (R - r * g.CL);
 }
 
 // Row of out / lse (token order) for row `row` of query tile q.
+template <bool S>
 __host__ __device__ __forceinline__ long long out_row(const Geom &g, const QTile &q, int row) {
-    return g.striped ? q.rank + (long long)g.P * (q.pos0 + row) : (long long)q.row0 + row;
+    return S ? q.rank + (long long)g.P * (q.pos0 + row) : (long long)q.row0 + row;
 }
 
 // Work item w -> (q tile, b, h).  Items are grouped by heads_per_group (b, h)
 // pairs so that concurrently running CTAs share K/V in L2; within a group the
 // query tiles come heaviest first under causal masking (latest positions).
+template <bool S>
 __host__ __device__ inline QTile work_item(const Geom &g, int w) {
     int BH = g.B * g.H;
     int G = g.heads_per_group;
@@ -297,7 +311,7 @@ __host__ __device__ inline QTile work_item(const Geom &g, int w) {
     int qi = rem / g_heads;
     int bh = grp * G + rem % g_heads;
     int qg = g.causal ? g.n_qtiles - 1 - qi : qi;
-    return q_tile(g, qg, bh / g.H, bh % g.H);
+    return q_tile<S>(g, qg, bh / g.H, bh % g.H);
 }
 
 // Is key position kp excluded for query position qp of batch item b?
@@ -341,6 +355,7 @@ __host__ __device__ inline int n_pairs(const Geom &g) {
 // that concurrently running CTAs share K/V in L2.  Phase 2 deals the lightest
 // levels of all heads, heaviest first: the items claimed last are the smallest
 // of the launch, so the CTAs finish within about one small item of each other.
+template <bool S>
 __host__ __device__ inline QPair work_pair(const Geom &g, int w) {
     const int BH = g.B * g.H, G = g.heads_per_group, np = n_pairs(g);
     const int tail = g.tail_levels < np ? g.tail_levels : np;
@@ -359,7 +374,7 @@ __host__ __device__ inline QPair work_pair(const Geom &g, int w) {
     }
     const int ppc = pairs_per_chunk(g), per = g.ring ? g.nqt_pc : g.n_qtiles;
     int c, i;
-    if (g.striped && g.causal) {
+    if (S && g.causal) {
         // a query at local index u of rank r sees P u + r + 1 keys: deal the
         // levels of all ranks together, last level and last rank first
         c = g.NC - 1 - pi % g.NC;
@@ -371,9 +386,9 @@ __host__ __device__ inline QPair work_pair(const Geom &g, int w) {
     }
     const int b = bh / g.H, h = bh % g.H;
     QPair p;
-    p.q0 = q_tile(g, c * per + 2 * i, b, h);
+    p.q0 = q_tile<S>(g, c * per + 2 * i, b, h);
     if (2 * i + 1 < per) {
-        p.q1 = q_tile(g, c * per + 2 * i + 1, b, h);
+        p.q1 = q_tile<S>(g, c * per + 2 * i + 1, b, h);
     } else {
         p.q1 = p.q0;
         p.q1.len = 0;
@@ -385,12 +400,14 @@ __host__ __device__ inline QPair work_pair(const Geom &g, int w) {
 
 // Next key tile of the pair's walk that one of its query tiles sees, with the
 // class for each (c1 = EMPTY when the pair holds one tile); false at the end.
-__host__ __device__ __forceinline__ bool pair_next(const Geom &g, const QPair &p, KWalk &w, KTile &k, int &c0, int &c1) {
+template <bool S>
+__host__ __device__ __forceinline__ bool pair_next(const Geom &g, const QPair &p, KWalk &w, KTile &k, int &c0,
+                                              int &c1) {
     const int q0_last = (int)p.q0.pos0 + p.q0.len - 1;
     const bool has1 = p.q1.len > 0;
     for (;;) {
         if (w.row >= w.chunk_end) {
-            if (!kwalk_next_chunk(g, w)) return false;
+            if (!kwalk_next_chunk<S>(g, w)) return false;
             continue;
         }
         const int row = w.row;
@@ -430,13 +447,14 @@ __host__ __device__ __forceinline__ bool pair_next(const Geom &g, const QPair &p
 }
 
 // Number of key tiles pair_next yields for pair p.
+template <bool S>
 __host__ __device__ inline int pair_count(const Geom &g, const QPair &p) {
-    if (!g.cls) return kwalk_count(g, p.span);   // the span's walk: both tiles see a tile the span sees
+    if (!g.cls) return kwalk_count<S>(g, p.span);   // the span's walk: both tiles see a tile the span sees
     KWalk w;
-    kwalk_begin(g, p.span, w);
+    kwalk_begin<S>(g, p.span, w);
     KTile k;
     int c0, c1, n = 0;
-    while (pair_next(g, p, w, k, c0, c1)) ++n;
+    while (pair_next<S>(g, p, w, k, c0, c1)) ++n;
     return n;
 }
 

@@ -38,9 +38,10 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
 // 128 rows of 64 columns starting at row R of head (h, b): a 4-D box at row R,
 // or, in the striped ring, a 5-D box {64, 1, 128, 1, 1} over the view
 // {d, P, CL, H, B} (row R = r CL + u is token r + P u: coordinates (r, u)).
+template <bool S>
 __device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap *map, const Geom &g, int col, int R,
                                               int h, int b, uint32_t bar) {
-    if (g.striped) {
+    if (S) {
         const int r = R / g.CL;
         tma_load_5d(dst, map, col, r, R - r * g.CL, h, b, bar);
     } else {

@@ -374,36 +374,65 @@ __device__ __forceinline__ void split_hi_lo(double c, float &hi, float &lo) {
     lo = __double2float_rn(c - (double)hi);
 }
 
-// Fast rounding of y = p + t (a rotated coordinate, computed in fp32 with
-// error at most err) to bfloat16: true when no bfloat16 rounding midpoint lies
-// within err of y, so that round(y) is the rounding of the exact value (Ziv's
-// rounding test).  The midpoint of y's bfloat16 interval is the only candidate
-// while err < 2^-10 |y|; |y - mid| is exact (same binade).
-__device__ __forceinline__ bool rounding_safe(float y, float err) {
-    const float mid = __uint_as_float((__float_as_uint(y) & 0xFFFF0000u) | 0x8000u);
-    return err <= fabsf(y) * 0x1p-10f && fabsf(y - mid) > err;
+// Two fp32 lanes per instruction (sm_100 f32x2 forms), each lane an IEEE
+// operation rounded to nearest.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(v.x, v.y);   // .x (low half) = v.x
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// The split cos and sin of one pair's angle, arranged for the two-lane forms:
+// lane 0 computes x0 c - x1 s, lane 1 computes x0 s + x1 c.
 struct RopeRowPair {
-    float ch, cl, sh, sl;   // split cos and sin of the pair's angle
+    float2 hi;     // (c_hi,  s_hi)
+    float2 hi_r;   // (-s_hi, c_hi)
+    float2 lo;     // (c_lo,  s_lo)
+    float2 lo_r;   // (-s_lo, c_lo)
 };
 
-// One output pair (y0, y1) = (x0 c - x1 s, x0 s + x1 c) of bfloat16 inputs by
-// the fast path; ok is false when either coordinate fails the rounding test.
-__device__ __forceinline__ void rot_fast(float x0, float x1, const RopeRowPair &k, uint16_t &o0, uint16_t &o1,
-                                         bool &ok) {
-    const float ax = fabsf(x0) + fabsf(x1);
-    const float h0 = fmaf(x0, k.ch, -(x1 * k.sh));         // exact products, one rounding
-    const float y0 = h0 + fmaf(x0, k.cl, -(x1 * k.sl));
-    const float h1 = fmaf(x0, k.sh, x1 * k.ch);
-    const float y1 = h1 + fmaf(x0, k.sl, x1 * k.cl);
-    // error bound: 2^-24 for each of the two roundings of the sum, 2^-38 |x|
-    // for the split of c, s and the low products; doubled
-    const float e0 = fmaf(0x1p-23f, fabsf(h0) + fabsf(y0), 0x1p-37f * ax);
-    const float e1 = fmaf(0x1p-23f, fabsf(h1) + fabsf(y1), 0x1p-37f * ax);
-    ok = rounding_safe(y0, e0) && rounding_safe(y1, e1);
-    o0 = __bfloat16_as_ushort(__float2bfloat16_rn(y0));
-    o1 = __bfloat16_as_ushort(__float2bfloat16_rn(y1));
+// One output pair of bfloat16 inputs (x0, x1), packed as two bfloat16.  The
+// rotation runs in fp32 on the split cos / sin: y = h + t with h = x0 c_hi -
+// x1 s_hi (the products exact, one rounding) and t the low-part terms.  Its
+// error is below E = 2^-22 |y| + 2^-36 (|x0| + |x1|) (the roundings of h and
+// y, 2^-24 each, and 2^-37 |x| for the low parts and the split), see the
+// exact path.  The packed result is safe when y - E' and y + E' (E' = E +
+// 2^-22 |y| covering their own rounding) round to the same bfloat16: every
+// value between them, the exact rotation included, rounds there as well
+// (Ziv's rounding test).  Returns false when the test cannot decide.
+__device__ __forceinline__ bool rot_fast2(float x0, float x1, const RopeRowPair &k, uint32_t &packed) {
+    const float2 xx0 = make_float2(x0, x0), xx1 = make_float2(x1, x1);
+    const float2 h = fma2(xx0, k.hi, mul2(xx1, k.hi_r));
+    const float2 t = fma2(xx0, k.lo, mul2(xx1, k.lo_r));
+    const float2 y = add2(h, t);
+    const float a = fmaf(0x1p-36f, fabsf(x0) + fabsf(x1), 0x1p-126f);   // absolute term (and denormals)
+    const float2 ay = make_float2(fabsf(y.x), fabsf(y.y));
+    const float2 e = fma2(ay, make_float2(0x1p-21f, 0x1p-21f), make_float2(a, a));
+    const uint32_t up = bf16x2_rn(add2(y, e));
+    const uint32_t dn = bf16x2_rn(add2(y, make_float2(-e.x, -e.y)));
+    packed = up;
+    return up == dn;
 }
 
 // bfloat16 with d a multiple of 8.  A CTA of 256 threads covers TP = 2048 / d
@@ -432,8 +461,13 @@ __global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
     for (int i = 0; i < 4; ++i) {
         double cs, sn;
         sincos_table(m * a.th.th[c0 + i], tab, sn, cs);
-        split_hi_lo(cs, k[i].ch, k[i].cl);
-        split_hi_lo(sn, k[i].sh, k[i].sl);
+        float ch, cl, sh, sl;
+        split_hi_lo(cs, ch, cl);
+        split_hi_lo(sn, sh, sl);
+        k[i].hi = make_float2(ch, sh);
+        k[i].hi_r = make_float2(-sh, ch);
+        k[i].lo = make_float2(cl, sl);
+        k[i].lo_r = make_float2(-sl, cl);
         exact[i][threadIdx.x] = make_double2(cs, sn);
     }
     const int rows = a.n * a.B * a.H;
@@ -466,35 +500,27 @@ __global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (py[u] == nullptr) continue;
-            uint16_t out[8];
+            uint32_t out[4];
             bool ok[4];
-            float x0[4], x1[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x0[i] = __uint_as_float(w[u][i] << 16);
-                x1[i] = __uint_as_float(w[u][i] & 0xFFFF0000u);
-                rot_fast(x0[i], x1[i], k[i], out[2 * i], out[2 * i + 1], ok[i]);
-            }
-            const bool all_ok = ok[0] && ok[1] && ok[2] && ok[3];
-            if (!all_ok) {
+            for (int i = 0; i < 4; ++i)
+                ok[i] = rot_fast2(__uint_as_float(w[u][i] << 16), __uint_as_float(w[u][i] & 0xFFFF0000u), k[i],
+                                  out[i]);
+            if (!(ok[0] && ok[1] && ok[2] && ok[3])) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (ok[i]) continue;
+                    const float x0 = __uint_as_float(w[u][i] << 16), x1 = __uint_as_float(w[u][i] & 0xFFFF0000u);
                     const double2 e = exact[i][threadIdx.x];
                     const Split4 c4 = split16(e.x), s4 = split16(e.y);
                     Split4 nc4;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) nc4.k[j] = -c4.k[j];
-                    out[2 * i] = rot_bf16(x0[i], c4, x1[i], s4);        // x0 cos - x1 sin
-                    out[2 * i + 1] = rot_bf16(x0[i], s4, x1[i], nc4);   // x0 sin - x1 (-cos)
+                    out[i] = (uint32_t)rot_bf16(x0, c4, x1, s4) |                // x0 cos - x1 sin
+                             ((uint32_t)rot_bf16(x0, s4, x1, nc4) << 16);       // x0 sin - x1 (-cos)
                 }
             }
-            uint4 o;
-            o.x = out[0] | ((uint32_t)out[1] << 16);
-            o.y = out[2] | ((uint32_t)out[3] << 16);
-            o.z = out[4] | ((uint32_t)out[5] << 16);
-            o.w = out[6] | ((uint32_t)out[7] << 16);
-            *reinterpret_cast<uint4 *>(py[u]) = o;
+            *reinterpret_cast<uint4 *>(py[u]) = make_uint4(out[0], out[1], out[2], out[3]);
         }
     }
 }

@@ -71,8 +71,8 @@ struct Cfg {
         B_VFULL = B_KEMPTY + KS,
         B_VEMPTY = B_VFULL + VS,     // PV_0(j) and PV_1(j) complete: V stage free
         B_SFULL = B_VEMPTY + VS,     // [x]: QK_x complete
-        B_PFULL = B_SFULL + 2,       // [x]: P_x stored by group x (128 arrivals)
-        B_PVDONE = B_PFULL + 2,      // [x]: PV_x complete (O_x may be rescaled)
+        B_PFULL = B_SFULL + 2,       // [2 x + h]: P_x of keys [64 h, 64 h + 64) stored by group x (128 arrivals)
+        B_PVDONE = B_PFULL + 4,      // [x]: PV_x complete (O_x may be rescaled)
         B_OFULL = B_PVDONE + 2,      // [x]: the item's last PV_x complete
         B_OEMPTY = B_OFULL + 2,      // [x]: group x has read O_x out (128 arrivals)
         B_DRAIN = B_OEMPTY + 2,
@@ -178,9 +178,9 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(bar(C::B_VFULL + i), 1);
             mbar_init(bar(C::B_VEMPTY + i), 1);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(C::B_PFULL + i), 128);
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(C::B_SFULL + x), 1);
-            mbar_init(bar(C::B_PFULL + x), 128);
             mbar_init(bar(C::B_PVDONE + x), 1);
             mbar_init(bar(C::B_OFULL + x), 1);
             mbar_init(bar(C::B_OEMPTY + x), 128);
@@ -353,16 +353,21 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 mma_commit_one(bar(C::B_SFULL + x));
             };
+            // P_x arrives in two halves of 64 keys: the products of the first half run
+            // while group x computes the exponentials of the second.
             auto pv = [&](int x, bool first) -> bool {
-                if (!warp_wait(bar(C::B_PFULL + x), pc[x] & 1, abort, a.err, lim)) return false;
-                ++pc[x];
-                tc_fence_after();   // P was written by the softmax warps' tcgen05.st
                 const uint64_t vd = vdesc0 + (uint64_t)(vst * STAGE16);
                 const uint32_t pa = tmem + C::S_COL + x * 128;
 #pragma unroll
-                for (int kk = 0; kk < TILE / 16; ++kk)
-                    mma_ts_one(tmem + C::O_COL + x * D, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), C::IDESC_PV,
-                               (first && kk == 0) ? 0u : 1u);
+                for (int h = 0; h < 2; ++h) {
+                    if (!warp_wait(bar(C::B_PFULL + 2 * x + h), pc[x] & 1, abort, a.err, lim)) return false;
+                    tc_fence_after();   // P was written by the softmax warps' tcgen05.st
+#pragma unroll
+                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                        mma_ts_one(tmem + C::O_COL + x * D, pa + kk * 8, vd + (uint64_t)((kk * 2048) >> 4),
+                                   C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                }
+                ++pc[x];
                 mma_commit_one(bar(C::B_PVDONE + x));
                 return true;
             };
@@ -540,6 +545,11 @@ __global__ void __launch_bounds__(320, 1)
                     alpha = fast_exp2(m_ref - m_new);   // 0 when m_ref = -inf
                     m_ref = m_new;
                 }
+                // O must be rescaled (rarely, when m moved) before this tile's first
+                // PV_x is issued; P is handed to the MMA warp in two halves of 64 keys,
+                // the first as soon as it is stored when no rescale is due, so that its
+                // products run while the second half's exponentials are computed.
+                const bool rescale_o = __any_sync(0xffffffffu, resc) && n > 0;
                 // p = 2^(s * scale * log2(e) - m), arguments two lanes at a time, sums in
                 // four two-lane accumulators; P (bf16) goes over the S columns already
                 // read, 16 columns (32 keys) at a time.
@@ -560,11 +570,16 @@ __global__ void __launch_bounds__(320, 1)
                         pk[j2] = pack_bf16(p0, p1);
                     }
                     tmem_st16(tmem + lane_addr + scol + c * 16, pk);
+                    if (c == 1 && !rescale_o) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(bar(C::B_PFULL + 2 * x));
+                    }
                 }
                 const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l = l * alpha + sum;
-                if (__any_sync(0xffffffffu, resc) && n > 0) {
-                    // O may be rescaled once PV of the previous tile has completed
+                if (rescale_o) {
+                    // once the previous tile's PV_x has completed
                     if (!warp_wait(bar(C::B_PVDONE + x), (tx - 1) & 1, abort, a.err, lim)) {
                         ok = false;
                         break;
@@ -582,7 +597,8 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL + x));
+                if (rescale_o) mbar_arrive(bar(C::B_PFULL + 2 * x));
+                mbar_arrive(bar(C::B_PFULL + 2 * x + 1));
                 ++tx;
                 ++n;
             }

@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller cases for counter captures)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override the workload's sequence length (smaller cases for counter captures)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-full", action="store_true",
@@ -112,6 +115,28 @@ def profiled_traffic(workload: str):
 # (kind::f16, cta_group::1) every 64 cycles, as measured on this part.
 TENSOR_FLOP_PER_CLK_SM = 2 * 128 * 128 * 16 // 64
 NUM_SMS = 152
+
+
+def graphed(fn, dev, enabled=True):
+    """fn captured into a CUDA graph (returned as a callable that replays it), or
+    fn itself when capture is disabled or refused."""
+    if not enabled:
+        return fn, False
+    try:
+        cur = torch.cuda.current_stream(dev)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(cur)
+        with torch.cuda.stream(cap):
+            fn()
+        cur.wait_stream(cap)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay, True
+    except Exception as e:  # noqa: BLE001
+        print(f"graph capture unavailable ({e}); timing eager launches", file=sys.stderr)
+        return fn, False
 
 
 def tensor_roofline(achieved, peaks, peak_src, clocks, timed_s):
@@ -337,21 +362,19 @@ def native_arm(args, w, rank, world, local_rank):
                                               inp.kpm is not None or inp.am is not None, False)
     ws = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=dev)
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        if rope:
-            ba.rope_apply(inp.q, x2=inp.k, base=w.rope_base, out=qr, out2=kr)
-            q_in, k_in = qr, kr
-        else:
-            q_in, k_in = inp.q, inp.k
-        if evs:
-            evs[1].record(stream)
+    def do_rope():
+        ba.rope_apply(inp.q, x2=inp.k, base=w.rope_base, out=qr, out2=kr)
+
+    def do_attn():
+        q_in, k_in = (qr, kr) if rope else (inp.q, inp.k)
         ba.ring_attn_fwd(q_in, k_in, inp.v, P=w.P, partition=w.partition, mode=args.mode,
                          key_padding_mask=inp.kpm, attn_mask=inp.am, causal=w.causal, out=out, lse=lse,
                          workspace=ws)
-        if evs:
-            evs[2].record(stream)
+
+    def step():
+        if rope:
+            do_rope()
+        do_attn()
 
     def barrier():
         if world > 1:
@@ -364,8 +387,47 @@ def native_arm(args, w, rank, world, local_rank):
     if rc != 0:
         raise RuntimeError(f"device status {rc} after warm-up")
 
+    # The step, and each of its two calls alone, captured once into CUDA graphs and
+    # replayed: the launches of the small workloads would otherwise be timed as host
+    # gaps between kernels (the 64K step is 21 ms of kernels either way).  Eager
+    # launches if the capture is refused.
+    graphs = {}
+    if not args.no_graph:
+        try:
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                step()
+            stream.wait_stream(cap)
+            for name, fn in (("step", step), ("attn", do_attn)) + ((("rope", do_rope),) if rope else ()):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                    fn()
+                graphs[name] = g
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001
+            print(f"graph capture unavailable ({e}); timing eager launches", file=sys.stderr)
+            graphs = {}
+
+    def run(name, fn):
+        if name in graphs:
+            graphs[name].replay()
+        else:
+            fn()
+
+    def timed(name, fn):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(args.steps):
+            run(name, fn)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        return a_.elapsed_time(b_) / args.steps
+
+    for name, fn in (("step", step), ("attn", do_attn)) + ((("rope", do_rope),) if rope else ()):
+        run(name, fn)   # each graph once before its timed loop
+    torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     if sampler:
@@ -374,15 +436,16 @@ def native_arm(args, w, rank, world, local_rank):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for s in range(args.steps):
-        step(evs[s])
+    for _ in range(args.steps):
+        run("step", step)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop() if sampler else None
     total_ms = t_start.elapsed_time(t_end)
-    attn_ms = [evs[s][1].elapsed_time(evs[s][2]) for s in range(args.steps)]
-    rope_ms = [evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)]
+    # the dominant kernel and RoPE alone, each over the same number of steps
+    attn_ms = [timed("attn", do_attn)]
+    rope_ms = [timed("rope", do_rope)] if rope else [0.0]
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
@@ -494,6 +557,7 @@ def native_arm(args, w, rank, world, local_rank):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": w.P,
                        "partition": w.partition, "causal": w.causal, "rope_base": w.rope_base,
                        "mode": args.mode, "visible_pairs": pairs, "flops_per_step": flops,
+                       "launch": "CUDA graph replay" if graphs else "eager",
                        "l2": "inputs (Q, K, V: 1.6 GB) larger than the 129 MB L2; no flush"},
             "tokens_per_s": world * w.B * w.T / (ms_step * 1e-3),
             "pct_of_bf16_peak": 100.0 * value / roof["peak"],
@@ -709,6 +773,7 @@ def merge_arm(args, w, rank, world, local_rank):
 
     for _ in range(args.warmup):
         step()
+    step, in_graph = graphed(step, dev, not args.no_graph)
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
@@ -736,6 +801,7 @@ def merge_arm(args, w, rank, world, local_rank):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": f"merge_rows_of_{w.name}", "rows": rows, "d": d, "bytes_per_step": nbytes,
+                       "launch": "CUDA graph replay" if in_graph else "eager",
                        "l2": f"partials ({2 * rows * d * 4 / 1e9:.2f} GB) far larger than the 129 MB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "merge_kernel",
@@ -763,6 +829,7 @@ def rope_arm(args, w, rank, world, local_rank):
 
     for _ in range(args.warmup):
         step()
+    step, in_graph = graphed(step, dev, not args.no_graph)
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
@@ -790,7 +857,7 @@ def rope_arm(args, w, rank, world, local_rank):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": f"rope_of_{w.name}", "B": w.B, "H": w.H, "T": w.T, "d": w.d, "base": base,
-                       "bytes_per_step": nbytes,
+                       "bytes_per_step": nbytes, "launch": "CUDA graph replay" if in_graph else "eager",
                        "l2": f"Q and K ({nbytes / 2e9:.2f} GB) larger than the 129 MB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "rope_bf16_kernel",
@@ -869,6 +936,8 @@ def main():
         w = w.replace(partition=args.partition)
     if args.heads:
         w = w.replace(H=args.heads, name=f"{w.name}_h{args.heads}")
+    if args.seq:
+        w = w.replace(T=args.seq, name=f"{w.name}_t{args.seq}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -270,8 +270,10 @@ struct RopeArgs {
     int B, H, T, d;
     const int32_t *positions;
     double pos_scale;       // Position Interpolation: angle = (position * pos_scale) * theta
+    unsigned *err;          // device error word (bounded waits of the bulk-copy kernel)
+    unsigned long long wait_limit_ns;
     Thetas th;
-    double tab_cos[64], tab_sin[64];   // cos, sin (n pi / 32), n = 0 .. 63 (sincos_table)
+    float4 tab[128];   // (cos hi, cos lo, sin hi, sin lo) of n pi / 64, n = 0 .. 127 (sincos_ff)
 };
 
 // fp64 -> bf16 with one rounding (ties to even): truncate to fp32, make the
@@ -289,24 +291,12 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// A double split into four floats of at most 16 significant bits each
-// (c ~= k0 + k1 + k2 + k3, relative error below 2^-48), so that the product
-// of any piece with a bfloat16 value (8 significant bits) is exact in fp32.
+// A value split into four floats of at most 16 significant bits each, so that
+// the product of any piece with a bfloat16 value (8 significant bits) is exact
+// in fp32 (split4_ff builds one from a float-float).
 struct Split4 {
     float k[4];
 };
-__device__ __forceinline__ Split4 split16(double c) {
-    Split4 r;
-    double rem = c;
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const float f = __uint_as_float(__float_as_uint(__double2float_rn(rem)) & 0xFFFFFF00u);
-        r.k[i] = f;
-        rem -= (double)f;
-    }
-    r.k[3] = __double2float_rn(rem);
-    return r;
-}
 
 // x0 * c - x1 * s (or x0 * s + x1 * c with the roles passed in) for bfloat16
 // x0, x1, rounded once to bfloat16.  Level-1 and level-2 products are exact
@@ -336,42 +326,98 @@ __device__ __forceinline__ uint16_t rot_bf16(float x0, const Split4 &a, float x1
     return (uint16_t)bits;
 }
 
-// sin and cos of an fp64 angle a, table-driven (Tang's method): a = n pi/32 + r
-// with |r| <= pi/64, r by a three-part Cody-Waite reduction (pi/32 split into
-// pieces of 27, 27 and 53 significant bits, so that n * piece is exact for
-// |n| < 2^26); sin r, cos r by their Taylor series (terms through r^9 / 9! and
-// r^8 / 8!: the next terms are below 2^-64 for |r| <= pi/64); then the angle
-// sum with the table entries cos, sin (n pi / 32), n mod 64.  Absolute error of
-// a few units of 2^-53.  Angles of 2^20 and beyond take sincos().
-__device__ __forceinline__ void sincos_table(double a, const double2 *tab, double &sn, double &cs) {
-    constexpr double K = 0x1.45f306dc9c883p+3;        // 32 / pi
-    constexpr double P1 = 0x1.921fb54000000p-4;       // pi / 32 = P1 + P2 + P3 (+ 2^-118)
-    constexpr double P2 = 0x1.10b4612000000p-34;
-    constexpr double P3 = -0x1.676733ae8fe48p-64;
-    if (!(fabs(a) < 1048576.0)) {
-        sincos(a, &sn, &cs);
+// A float-float value hi + lo (|lo| at most about 2^-24 |hi|): 48 significant
+// bits carried by the fp32 pipe, which runs far faster than the fp64 one.
+struct FF {
+    float hi, lo;
+};
+
+// x y: the product of the high parts split exactly by an fma, plus the cross
+// terms (relative error about 2^-47).
+__device__ __forceinline__ FF ff_mul(FF x, FF y) {
+    const float p = x.hi * y.hi;
+    const float e = fmaf(x.hi, y.hi, -p);
+    return FF{p, fmaf(x.hi, y.lo, fmaf(x.lo, y.hi, e))};
+}
+
+// x + y: Knuth's two-sum of the high parts plus the low parts, renormalised.
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+    const float s = x.hi + y.hi;
+    const float bb = s - x.hi;
+    const float e = (x.hi - (s - bb)) + (y.hi - bb);
+    const float l = e + (x.lo + y.lo);
+    const float h = s + l;
+    return FF{h, l - (h - s)};
+}
+
+__device__ __forceinline__ FF ff_neg(FF x) { return FF{-x.hi, -x.lo}; }
+
+// sin and cos of an fp64 angle a to about 2^-48 absolute, table-driven (Tang's
+// method).  In fp64 only the reduction: a = n pi/64 + r, |r| <= pi/128, with
+// pi/64 split into pieces of 27, 27 and 24 significant bits (n * piece exact
+// for |n| < 2^23); r goes to float-float, the third piece's product folded
+// into its low part.  Then in float-float on the fp32 pipe: the Taylor series
+// of sin r and cos r (the r^3/3! and r^2/2! terms carried with their rounding
+// errors, r^5/5!, r^7/7!, r^4/4!, r^6/6! in fp32, the next terms below 2^-60),
+// and the angle sum with the table entries cos, sin (n pi / 64), n mod 128.
+// Angles of 2^19 and beyond take sincos() in fp64.
+__device__ __forceinline__ void sincos_ff(double a, const float4 *tab, FF &sn, FF &cs) {
+    constexpr double K = 0x1.45f306dc9c883p+4;        // 64 / pi
+    constexpr double Q1 = 0x1.921fb54000000p-5;       // pi / 64 = Q1 + Q2 + Q3 (+ 5e-28)
+    constexpr double Q2 = 0x1.10b4612000000p-35;
+    constexpr float Q3 = -0x1.676734p-65f;
+    constexpr float K6 = 0x1.555556p-3f;              // 1/6 = K6 + K6E (+ 2^-52)
+    constexpr float K6E = -0x1.555556p-28f;
+    if (!(fabs(a) < 524288.0)) {
+        double sv, cv;
+        sincos(a, &sv, &cv);
+        const float sh = __double2float_rn(sv), ch = __double2float_rn(cv);
+        sn = FF{sh, __double2float_rn(sv - (double)sh)};
+        cs = FF{ch, __double2float_rn(cv - (double)ch)};
         return;
     }
-    const double n = rint(a * K);
-    double r = fma(-n, P1, a);
-    r = fma(-n, P2, r);
-    r = fma(-n, P3, r);
-    const double z = r * r;
-    // sin r = r - r^3/3! + r^5/5! - r^7/7! + r^9/9!;  cos r = 1 - r^2/2! + ... + r^8/8!
-    const double sp = fma(z, fma(z, fma(z, 1.0 / 362880.0, -1.0 / 5040.0), 1.0 / 120.0), -1.0 / 6.0);
-    const double sr = fma(r * z, sp, r);
-    const double cp = fma(z, fma(z, fma(z, 1.0 / 40320.0, -1.0 / 720.0), 1.0 / 24.0), -0.5);
-    const double cr = fma(z, cp, 1.0);
-    const double2 t = tab[(int)((long long)n & 63)];   // (cos, sin) of (n mod 64) pi / 32
-    cs = fma(t.x, cr, -t.y * sr);
-    sn = fma(t.y, cr, t.x * sr);
+    const double nd = rint(a * K);
+    double r = fma(-nd, Q1, a);
+    r = fma(-nd, Q2, r);
+    const int n = (int)nd;
+    const float rh = __double2float_rn(r);
+    const float rl = fmaf(-(float)n, Q3, __double2float_rn(r - (double)rh));
+    const float p = rh * rh, pe = fmaf(rh, rh, -p);     // rh^2 = p + pe exactly
+    // sin r = r - r^3/6 + r^5/120 - r^7/5040
+    const float c3 = p * rh, c3e = fmaf(p, rh, -c3);     // rh^3 = c3 + c3e + pe rh
+    const float l3 = c3e + fmaf(pe, rh, 3.f * p * rl);   // with the 3 rh^2 rl term of r^3
+    const float t3h = c3 * K6, t3e = fmaf(c3, K6, -t3h);
+    const float t3l = t3e + fmaf(c3, K6E, l3 * K6);      // r^3 / 6 = t3h + t3l
+    const float t57 = rh * p * p * fmaf(p, -1.f / 5040.f, 1.f / 120.f);
+    const float s1 = rh - t3h, s1e = (rh - s1) - t3h;    // exact (|rh| >= |t3h|)
+    const FF sin_r{s1, ((s1e + rl) - t3l) + t57};
+    // cos r = 1 - r^2/2 + r^4/24 - r^6/720
+    const float t2h = 0.5f * p, t2l = 0.5f * fmaf(2.f * rh, rl, pe);
+    const float t46 = p * p * fmaf(p, -1.f / 720.f, 1.f / 24.f);
+    const float c1 = 1.f - t2h, c1e = (1.f - c1) - t2h;  // exact
+    const FF cos_r{c1, (c1e - t2l) + t46};
+    const float4 t = tab[n & 127];                       // (cos hi, cos lo, sin hi, sin lo) of (n mod 128) pi/64
+    const FF tc{t.x, t.y}, ts{t.z, t.w};
+    cs = ff_add(ff_mul(tc, cos_r), ff_neg(ff_mul(ts, sin_r)));
+    sn = ff_add(ff_mul(ts, cos_r), ff_mul(tc, sin_r));
 }
 
 // c = hi + lo with hi of 16 significant bits (its product with a bfloat16 is
 // exact in fp32) and lo the fp32 rounding of the rest (|lo| < 2^-15 |c|).
-__device__ __forceinline__ void split_hi_lo(double c, float &hi, float &lo) {
-    hi = __uint_as_float(__float_as_uint(__double2float_rn(c)) & 0xFFFFFF00u);
-    lo = __double2float_rn(c - (double)hi);
+__device__ __forceinline__ void split_hi_lo(FF c, float &hi, float &lo) {
+    hi = __uint_as_float(__float_as_uint(c.hi) & 0xFFFFFF00u);
+    lo = (c.hi - hi) + c.lo;
+}
+
+// c as four pieces of at most 16 significant bits whose sum is exactly
+// c.hi + c.lo, so that each product with a bfloat16 is exact in fp32.
+__device__ __forceinline__ Split4 split4_ff(FF c) {
+    Split4 r;
+    r.k[0] = __uint_as_float(__float_as_uint(c.hi) & 0xFFFFFF00u);
+    r.k[1] = c.hi - r.k[0];
+    r.k[2] = __uint_as_float(__float_as_uint(c.lo) & 0xFFFFFF00u);
+    r.k[3] = c.lo - r.k[2];
+    return r;
 }
 
 // Two fp32 lanes per instruction (sm_100 f32x2 forms), each lane an IEEE
@@ -435,32 +481,15 @@ __device__ __forceinline__ bool rot_fast2(float x0, float x1, const RopeRowPair 
     return up == dn;
 }
 
-// bfloat16 with d a multiple of 8.  A CTA of 256 threads covers TP = 2048 / d
-// positions x d columns; thread (t, g) owns the four pairs 4g .. 4g+3 at
-// position t.  It computes their angles' cos and sin once (fp64, table-driven)
-// and rotates those pairs in every row of the CTA's share of the (tensor, b, h)
-// rows, four rows' 16-byte loads in flight at a time.  The rotation runs in
-// fp32 with a rounding test; the rare coordinate the test cannot decide is
-// recomputed exactly (rot_bf16), so every output is the exact rotation rounded
-// once to bfloat16.
-template <bool VEC>
-__global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
-    __shared__ double2 tab[64];
-    __shared__ double2 exact[4][256];   // fp64 (cos, sin) of each thread's pairs, for the exact path
-    if (threadIdx.x < 64) tab[threadIdx.x] = make_double2(a.tab_cos[threadIdx.x], a.tab_sin[threadIdx.x]);
-    __syncthreads();
-    const int G = a.d / 8;
-    const int TP = 256 / G;
-    const int tl = threadIdx.x / G, grp = threadIdx.x % G;
-    const long long t = (long long)blockIdx.x * TP + tl;
-    if (tl >= TP || t >= a.T) return;
-    const int c0 = grp * 4;
+// The four pairs 4 c0 .. 4 c0 + 3 at position t: cos and sin of their angles
+// (float-float), split for the fast path (k) and kept whole for the exact one.
+__device__ __forceinline__ void rope_setup(const RopeArgs &a, const float4 *tab, long long t, int c0,
+                                           RopeRowPair (&k)[4], float4 (&exact)[4][256]) {
     const double m = (a.positions ? (double)a.positions[t] : (double)t) * a.pos_scale;
-    RopeRowPair k[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        double cs, sn;
-        sincos_table(m * a.th.th[c0 + i], tab, sn, cs);
+        FF cs, sn;
+        sincos_ff(m * a.th.th[c0 + i], tab, sn, cs);
         float ch, cl, sh, sl;
         split_hi_lo(cs, ch, cl);
         split_hi_lo(sn, sh, sl);
@@ -468,12 +497,69 @@ __global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
         k[i].hi_r = make_float2(-sh, ch);
         k[i].lo = make_float2(cl, sl);
         k[i].lo_r = make_float2(-sl, cl);
-        exact[i][threadIdx.x] = make_double2(cs, sn);
+        exact[i][threadIdx.x] = make_float4(cs.hi, cs.lo, sn.hi, sn.lo);
     }
+}
+
+// Rotate four bfloat16 pairs (one 16-byte word) by the fast path, falling back
+// to the exact rotation for a pair whose rounding the test cannot decide.
+__device__ __forceinline__ uint4 rope_rotate(const uint32_t (&w)[4], const RopeRowPair (&k)[4],
+                                             const float4 (&exact)[4][256]) {
+    uint32_t out[4];
+    bool ok[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        ok[i] = rot_fast2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u), k[i], out[i]);
+    if (!(ok[0] && ok[1] && ok[2] && ok[3])) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (ok[i]) continue;
+            const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
+            const float4 e = exact[i][threadIdx.x];
+            const Split4 c4 = split4_ff(FF{e.x, e.y}), s4 = split4_ff(FF{e.z, e.w});
+            Split4 nc4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) nc4.k[j] = -c4.k[j];
+            out[i] = (uint32_t)rot_bf16(x0, c4, x1, s4) |                // x0 cos - x1 sin
+                     ((uint32_t)rot_bf16(x0, s4, x1, nc4) << 16);       // x0 sin - x1 (-cos)
+        }
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Rows [r_begin, r_end) of the (tensor, b, h) list given to a CTA (blockIdx.y).
+__device__ __forceinline__ void rope_rows(const RopeArgs &a, int &r_begin, int &r_end) {
     const int rows = a.n * a.B * a.H;
     const int per = (rows + gridDim.y - 1) / gridDim.y;
-    const int r_begin = blockIdx.y * per;
-    const int r_end = r_begin + per < rows ? r_begin + per : rows;
+    r_begin = blockIdx.y * per;
+    r_end = r_begin + per < rows ? r_begin + per : rows;
+}
+
+// bfloat16 with d a multiple of 8.  A CTA of 256 threads covers TP = 2048 / d
+// positions x d columns; thread (t, g) owns the four pairs 4g .. 4g+3 at
+// position t.  It computes their angles' cos and sin once (float-float,
+// table-driven) and rotates those pairs in every row of the CTA's share of the
+// (tensor, b, h) rows, four rows' 16-byte loads in flight at a time.  The
+// rotation runs in fp32 with a rounding test; the rare coordinate the test
+// cannot decide is recomputed exactly (rot_bf16), so every output is the exact
+// rotation rounded once to bfloat16.  (Strided rows; contiguous ones take the
+// bulk-copy kernel below.)
+template <bool VEC>
+__global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
+    __shared__ float4 tab[128];
+    __shared__ float4 exact[4][256];   // float-float (cos, sin) of each thread's pairs, for the exact path
+    if (threadIdx.x < 128) tab[threadIdx.x] = a.tab[threadIdx.x];
+    __syncthreads();
+    const int G = a.d / 8;
+    const int TP = 256 / G;
+    const int tl = threadIdx.x / G, grp = threadIdx.x % G;
+    const long long t = (long long)blockIdx.x * TP + tl;
+    if (tl >= TP || t >= a.T) return;
+    const int c0 = grp * 4;
+    RopeRowPair k[4];
+    rope_setup(a, tab, t, c0, k, exact);
+    int r_begin, r_end;
+    rope_rows(a, r_begin, r_end);
     constexpr int U = 4;
     for (int r0 = r_begin; r0 < r_end; r0 += U) {
         uint32_t w[U][4];
@@ -500,27 +586,131 @@ __global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (py[u] == nullptr) continue;
-            uint32_t out[4];
-            bool ok[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                ok[i] = rot_fast2(__uint_as_float(w[u][i] << 16), __uint_as_float(w[u][i] & 0xFFFF0000u), k[i],
-                                  out[i]);
-            if (!(ok[0] && ok[1] && ok[2] && ok[3])) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (ok[i]) continue;
-                    const float x0 = __uint_as_float(w[u][i] << 16), x1 = __uint_as_float(w[u][i] & 0xFFFF0000u);
-                    const double2 e = exact[i][threadIdx.x];
-                    const Split4 c4 = split16(e.x), s4 = split16(e.y);
-                    Split4 nc4;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) nc4.k[j] = -c4.k[j];
-                    out[i] = (uint32_t)rot_bf16(x0, c4, x1, s4) |                // x0 cos - x1 sin
-                             ((uint32_t)rot_bf16(x0, s4, x1, nc4) << 16);       // x0 sin - x1 (-cos)
-                }
-            }
-            *reinterpret_cast<uint4 *>(py[u]) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4 *>(py[u]) = rope_rotate(w[u], k, exact);
+        }
+    }
+}
+
+// bfloat16, d a multiple of 8, contiguous rows (sT = d): the CTA's positions
+// are one contiguous block of TP d 2 = 4096 bytes in every row, which one
+// thread streams into a ring of ROPE_RING shared-memory slots with bulk copies
+// (cp.async.bulk, completion counted on a "full" mbarrier per slot), ROPE_RING
+// rows ahead of the rotation.  Each thread reads its 16 bytes of a slot,
+// rotates them as in rope_bf16_kernel and stores the result; each warp then
+// signals the slot's "empty" mbarrier, and the streaming thread refills the
+// slot once all eight warps have.  Many rows' bytes are in flight per CTA
+// without registers held for them, and no block-wide barrier is taken per
+// row.  Every wait is bounded: on expiry the thread records the timeout and
+// stops (the streaming thread first lets its copies in flight land).
+constexpr int ROPE_RING = 6;   // 24 KB of slots (even: rows go two by two); three CTAs an SM keep 72 KB in flight
+__global__ void __launch_bounds__(256, 3) rope_bf16_bulk_kernel(const RopeArgs a) {
+    __shared__ float4 tab[128];
+    __shared__ float4 exact[4][256];
+    __shared__ __align__(128) uint4 ring[ROPE_RING][256];
+    __shared__ __align__(8) uint64_t full[ROPE_RING], empty[ROPE_RING];
+    __shared__ int abort_flag;
+    if (threadIdx.x < 128) tab[threadIdx.x] = a.tab[threadIdx.x];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < ROPE_RING; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 8);   // one arrival per warp
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int G = a.d / 8;
+    const int TP = 256 / G;
+    const int tl = threadIdx.x / G, grp = threadIdx.x % G;
+    const long long t0 = (long long)blockIdx.x * TP;
+    const long long t = t0 + tl;
+    const bool valid = tl < TP && t < a.T;   // (256 = TP G exactly when d divides 2048)
+    const int tp = a.T - t0 < TP ? (int)(a.T - t0) : TP;   // positions of this block
+    const uint32_t bytes = (uint32_t)tp * (uint32_t)a.d * 2u;
+    int r_begin, r_end;
+    rope_rows(a, r_begin, r_end);
+    const int BH = a.B * a.H;
+    // row r = (tensor ti, b, h): positions t0 .. t0 + tp - 1 of head (b, h)
+    auto src = [&](int r) -> const void * {
+        const int ti = r / BH, bh = r % BH, b = bh / a.H, h = bh % a.H;
+        return static_cast<const __nv_bfloat16 *>(a.x[ti]) + b * a.sB[ti] + h * a.sH[ti] + t0 * a.sT[ti];
+    };
+    auto issue = [&](int slot, int r) {
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(bar, bytes);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_u32(&ring[slot][0])),
+            "l"(src(r)), "r"(bytes), "r"(bar)
+            : "memory");
+    };
+    int issued = 0;   // rows issued (thread 0)
+    if (threadIdx.x == 0)
+        for (; issued < ROPE_RING && r_begin + issued < r_end; ++issued) issue(issued, r_begin + issued);
+    RopeRowPair k[4];
+    if (valid) rope_setup(a, tab, t, grp * 4, k, exact);
+    // output row pointer, advanced row by row: (ti, bh) of row r_begin, then bh + 1 ...
+    int ti = r_begin / BH, bh = r_begin % BH;
+    const long long step = (long long)a.T * a.d;
+    __nv_bfloat16 *py = static_cast<__nv_bfloat16 *>(a.y[ti]) + ((long long)bh * a.T + t) * a.d + grp * 8;
+    auto advance = [&]() {   // py to the next row
+        if (++bh == BH) {
+            bh = 0;
+            ++ti;
+            py = static_cast<__nv_bfloat16 *>(a.y[ti < a.n ? ti : 0]) + (long long)t * a.d + grp * 8;
+        } else {
+            py += step;
+        }
+    };
+    // refill slot with row r_begin + issued (= the row ROPE_RING after the one just read)
+    // once every warp has read it; false when the wait expired
+    auto refill = [&](int slot, uint32_t ph) -> bool {
+        if (issued >= r_end - r_begin) return true;
+        if (!mbar_wait(smem_u32(&empty[slot]), ph, &abort_flag, a.err, a.wait_limit_ns)) return false;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic reads before the copy's writes
+        issue(slot, r_begin + issued);
+        ++issued;
+        return true;
+    };
+    // two rows (two slots) per iteration: their rotations are independent work
+    const int nrows = r_end - r_begin;
+    for (int i = 0; i < nrows; i += 2) {
+        const bool two = i + 1 < nrows;
+        const int s0 = i % ROPE_RING, s1 = (i + 1) % ROPE_RING;   // ROPE_RING is even
+        const uint32_t ph0 = (uint32_t)(i / ROPE_RING) & 1u, ph1 = (uint32_t)((i + 1) / ROPE_RING) & 1u;
+        // warp-uniform verdicts, so that a warp leaves the loop whole
+        bool got = mbar_wait(smem_u32(&full[s0]), ph0, &abort_flag, a.err, a.wait_limit_ns);
+        if (got && two) got = mbar_wait(smem_u32(&full[s1]), ph1, &abort_flag, a.err, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, got)) break;
+        __nv_bfloat16 *py0 = py;
+        advance();
+        __nv_bfloat16 *py1 = py;
+        if (two) advance();
+        if (valid) {
+            const uint4 v0 = ring[s0][threadIdx.x];
+            const uint4 v1 = two ? ring[s1][threadIdx.x] : v0;
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint4 o0 = rope_rotate(w0, k, exact);
+            const uint4 o1 = rope_rotate(w1, k, exact);
+            __stcs(reinterpret_cast<uint4 *>(py0), o0);
+            if (two) __stcs(reinterpret_cast<uint4 *>(py1), o1);
+        }
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            mbar_arrive(smem_u32(&empty[s0]));
+            if (two) mbar_arrive(smem_u32(&empty[s1]));
+        }
+        bool stop = false;
+        if (threadIdx.x == 0) stop = !refill(s0, ph0) || (two && !refill(s1, ph1));
+        if (__any_sync(0xffffffffu, stop)) break;
+    }
+    if (threadIdx.x == 0 && abort_flag) {
+        // let the copies still in flight land before the CTA exits
+        volatile int never = 0;
+        for (int j = 0; j < ROPE_RING; ++j) {
+            const int n_use = (issued - j + ROPE_RING - 1) / ROPE_RING;   // fills of slot j
+            if (j < issued && n_use > 0)
+                mbar_wait(smem_u32(&full[j]), (uint32_t)(n_use - 1) & 1u, &never, nullptr, 200000000ull);
         }
     }
 }
@@ -658,14 +848,20 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
     a.d = d;
     a.positions = pos;
     a.pos_scale = pos_scale > 0.f ? (double)pos_scale : 1.0;   // a float times an int32 is exact in fp64
+    {
+        const int dev = current_device();
+        a.err = dev >= 0 ? g_err_ptr[dev] : nullptr;
+        a.wait_limit_ns = kWaitLimitNs;
+    }
     if ((long long)T * d == 0 || B == 0 || H == 0) return BA_OK;
     const int threads = 256;
     if (dtype == BA_BF16 && d % 8 == 0) {
-        // the table of sincos_table: cos, sin (n pi / 32), from the first octant by symmetry
+        // the table of sincos_ff: cos, sin (n pi / 64) as float-float, from the first
+        // quadrant by symmetry
         const long double pi = 3.14159265358979323846264338327950288L;
-        for (int n = 0; n < 64; ++n) {
-            const int q = n / 16, m = n % 16;   // angle = q pi/2 + m pi/32
-            long double c = cosl(pi * m / 32), sv = sinl(pi * m / 32);
+        for (int n = 0; n < 128; ++n) {
+            const int q = n / 32, m = n % 32;   // angle = q pi/2 + m pi/64
+            long double c = cosl(pi * m / 64), sv = sinl(pi * m / 64);
             if (m == 0) {
                 c = 1;
                 sv = 0;
@@ -675,8 +871,8 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
                 c = -sv;
                 sv = t;
             }
-            a.tab_cos[n] = (double)c;
-            a.tab_sin[n] = (double)sv;
+            const float ch = (float)c, sh = (float)sv;
+            a.tab[n] = make_float4(ch, (float)(c - ch), sh, (float)(sv - sh));
         }
         const int per_cta = 2048 / d;                       // positions per CTA
         const long long gx = ((long long)T + per_cta - 1) / per_cta;
@@ -689,7 +885,11 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
         if (gy < 1) gy = 1;
         if (gx > 0x7fffffffLL) return BA_ERR_SHAPE;
         const dim3 grid((unsigned)gx, (unsigned)gy);
-        if (vec)
+        bool rows_contiguous = vec;
+        for (int i = 0; i < a.n; ++i) rows_contiguous = rows_contiguous && a.sT[i] == d;
+        if (rows_contiguous)
+            rope_bf16_bulk_kernel<<<grid, threads, 0, s>>>(a);
+        else if (vec)
             rope_bf16_kernel<true><<<grid, threads, 0, s>>>(a);
         else
             rope_bf16_kernel<false><<<grid, threads, 0, s>>>(a);

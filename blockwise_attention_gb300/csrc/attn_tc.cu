@@ -142,11 +142,58 @@ __device__ __noinline__ uint32_t keep_bits(const Geom &g, int b, long long qpos,
     return m;
 }
 
+// The keys of key tile kt (positions kpos0 .. kpos0 + klen - 1) that the query
+// at global position qpos may see, as four 32-bit masks (bit i of m[c] for key
+// 32 c + i): inside the tile, not in the causal future, not padded, not
+// forbidden by attn_mask.  Every mask byte the tile needs is loaded before any
+// is used (up to sixteen independent 16-byte loads), so the call costs about
+// one load latency, and it is made before the tile's scores are waited for.
+// The kernels that use it (PF: launches with masks, striped ranks, or short
+// walks, where PARTIAL tiles are a sizeable share) trade this for a slightly
+// different hot loop, measured about 1 % slower on the 64K prefill, whose
+// walks are long and nearly all FULL.
+struct Keep4 {
+    uint32_t m[4];
+};
+
+__device__ __noinline__ Keep4 keep_bits4(const Geom &g, int b, long long qpos, bool row_valid, long long kpos0,
+                                         int klen) {
+    Keep4 r;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int n = klen - 32 * c;
+        uint32_t m = n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : (1u << n) - 1u);
+        if (g.causal) {
+            const long long lim = qpos - kpos0 - 32 * c;   // key 32 c + i lies in the future when i > lim
+            if (lim < 0) m = 0u;
+            else if (lim < 31) m &= (2u << lim) - 1u;
+        }
+        r.m[c] = m;
+    }
+    if (!row_valid) return r;   // rows past the tile end are never stored; their mask rows may not exist
+    uint32_t ek[4] = {0u, 0u, 0u, 0u}, ea[4] = {0u, 0u, 0u, 0u};
+    if (g.kpm) {
+        const uint8_t *p = g.kpm + b * g.kpm_ld + kpos0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (klen > 32 * c) ek[c] = excl_bits(p + 32 * c, klen - 32 * c);
+    }
+    if (g.am) {
+        const uint8_t *p = g.am + qpos * g.am_ld + kpos0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (klen > 32 * c) ea[c] = excl_bits(p + 32 * c, klen - 32 * c);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) r.m[c] &= ~(ek[c] | ea[c]);
+    return r;
+}
+
 // ----------------------------------------------------------------------------
 // Kernel
 // ----------------------------------------------------------------------------
 
-template <int D, bool S>
+template <int D, bool S, bool PF>
 __global__ void __launch_bounds__(320, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tq,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -496,6 +543,13 @@ __global__ void __launch_bounds__(320, 1)
                     kt.len = (int)(dy & 0xffffu);
                     kt.cls = (int)((dy >> (16 + 4 * x)) & 15u);
                 }
+                // FULL tiles need no predicate; PARTIAL ones, and tiles EMPTY for this
+                // group's rows (seen only by the other tile of the pair), are masked.
+                const bool masked = kt.cls != BA_TILE_FULL || kt.len < TILE;
+                Keep4 keep;
+                if constexpr (PF) {
+                    if (masked) keep = keep_bits4(g, qt.b, qpos, row < qt.len, kt.pos0, kt.len);
+                }
                 if (!warp_wait(bar(C::B_SFULL + x), sx & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
@@ -513,16 +567,18 @@ __global__ void __launch_bounds__(320, 1)
                     for (int j2 = 0; j2 < TILE; ++j2) s[j2] = __uint_as_float(r[j2]);
                 }
 
-                // FULL tiles need no predicate; PARTIAL ones, and tiles EMPTY for this
-                // group's rows (seen only by the other tile of the pair), are masked.
-                if (kt.cls != BA_TILE_FULL || kt.len < TILE) {
-                    const bool row_valid = row < qt.len;   // rows past the tile end are never stored
+                if (masked) {
 #pragma unroll
                     for (int c = 0; c < TILE / 32; ++c) {
-                        const uint32_t keep = keep_bits(g, qt.b, qpos, row_valid, kt.pos0, kt.len, c * 32);
+                        uint32_t kb;
+                        if constexpr (PF) {
+                            kb = keep.m[c];
+                        } else {
+                            kb = keep_bits(g, qt.b, qpos, row < qt.len, kt.pos0, kt.len, c * 32);
+                        }
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (!((keep >> i) & 1u)) s[c * 32 + i] = -INFINITY;
+                            if (!((kb >> i) & 1u)) s[c * 32 + i] = -INFINITY;
                     }
                 }
                 // Row maximum first (8 independent chains of three-input maxima, then a
@@ -644,16 +700,31 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-template <int D, bool S>
-int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
+template <int D, bool S, bool PF>
+int launch_dpf(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
     using C = Cfg<D>;
     static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, S, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return BA_ERR_CUDA;
     int grid = a.g.n_items < num_sms ? a.g.n_items : num_sms;
-    attn_tc_kernel<D, S><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
+    attn_tc_kernel<D, S, PF><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
+}
+
+// Masks are prefetched (keep_bits4 before the scores are waited for) when
+// PARTIAL tiles are a sizeable share of the walks: with masks, with striped
+// ranks (a diagonal in every block), or when a head has fewer than 256 key
+// tiles (T < 32K: the causal diagonal tiles are one in about 17 of a walk
+// or more).
+template <int D, bool S>
+int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
+    if constexpr (S) {
+        return launch_dpf<D, S, true>(a, m, num_sms, s);
+    } else {
+        const bool pf = a.g.kpm != nullptr || a.g.am != nullptr || a.g.n_ktiles < 256;
+        return pf ? launch_dpf<D, S, true>(a, m, num_sms, s) : launch_dpf<D, S, false>(a, m, num_sms, s);
+    }
 }
 
 }  // namespace

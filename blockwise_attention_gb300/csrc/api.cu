@@ -155,20 +155,43 @@ int heads_per_group(int B, int H, long long keys, int d, int dtype) {
 // small kernels
 // ---------------------------------------------------------------------------
 
+// Exclusion bytes (nonzero = excluded) of keys [j0, j0 + 16) of a mask row,
+// of which the first n exist: one 16-byte load when they all exist and the
+// row is aligned, byte loads otherwise.
+__device__ __forceinline__ uint4 mask16(const uint8_t *p, int n) {
+    if (n >= 16 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) return __ldg(reinterpret_cast<const uint4 *>(p));
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int i = 0; i < 16 && i < n; ++i) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Class of every (b, q tile, k tile) of the walk geometry: one CTA per tile
-// pair, one thread per query row.
+// pair, one thread per query row, which reads its key-padding and attn_mask
+// bytes 16 keys at a time.  (Masks are never taken with striped ranks, so the
+// positions are the tokens.)
 __global__ void tile_class_kernel(const Geom g, int8_t *cls) {
     const int kg = blockIdx.x, qg = blockIdx.y, b = blockIdx.z;
-    const QTile q = q_tile<false>(g, qg, b, 0);   // masks: never striped
+    const QTile q = q_tile<false>(g, qg, b, 0);
     const KTile k = k_tile_by_id(g, kg);
     const int i = threadIdx.x;
     int any = 0, all = 1;
     if (i < q.len) {
         const long long qp = q.pos0 + i;
-        for (int j = 0; j < k.len; ++j) {
-            const bool vis = !excluded(g, b, qp, k.pos0 + j);
-            any |= vis;
-            all &= vis;
+        const uint8_t *kr = g.kpm ? g.kpm + b * g.kpm_ld + k.pos0 : nullptr;
+        const uint8_t *ar = g.am ? g.am + qp * g.am_ld + k.pos0 : nullptr;
+        const long long lim = g.causal ? qp - k.pos0 : (long long)TILE;   // keys j > lim lie in the future
+        for (int j0 = 0; j0 < k.len; j0 += 16) {
+            const int n = k.len - j0;
+            const uint4 ek = kr ? mask16(kr + j0, n) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 ea = ar ? mask16(ar + j0, n) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t e[4] = {ek.x | ea.x, ek.y | ea.y, ek.z | ea.z, ek.w | ea.w};
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                if (jj >= n) break;
+                const bool vis = ((e[jj >> 2] >> (8 * (jj & 3))) & 0xffu) == 0u && j0 + jj <= lim;
+                any |= vis;
+                all &= vis;
+            }
         }
     }
     any = __syncthreads_or(any);

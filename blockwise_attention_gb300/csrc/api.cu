@@ -1402,9 +1402,10 @@ int check_bwd_common(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_te
 
 }  // namespace
 
+// 256 bytes of item counters for the persistent tensor-core kernels, then D.
 size_t attn_block_bwd_workspace_size(int B, int H, int Lq) {
     if (B < 0 || H < 0 || Lq < 0) return 0;
-    return align256((size_t)4 * (size_t)B * (size_t)H * (size_t)Lq);
+    return 256 + align256((size_t)4 * (size_t)B * (size_t)H * (size_t)Lq);
 }
 
 int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tensor dout, const float *lse, int B,
@@ -1449,7 +1450,9 @@ int attn_block_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tens
     a.k = tref(k);
     a.v = tref(v);
     a.lse = lse;
-    a.D = static_cast<float *>(ws.ptr);
+    a.sched = static_cast<unsigned *>(ws.ptr);
+    a.D = reinterpret_cast<float *>(static_cast<uint8_t *>(ws.ptr) + 256);
+    a.heads_per_group = heads_per_group(B, H, Lq > Lk ? Lq : Lk, d, dtype);
     a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
     a.dq = dq;
     a.dk = dk;
@@ -1507,7 +1510,9 @@ int ring_attn_bwd(ba_tensor q, ba_tensor k, ba_tensor v, ba_tensor out, ba_tenso
     a.k = tref(k);
     a.v = tref(v);
     a.lse = lse;
-    a.D = static_cast<float *>(ws.ptr);
+    a.sched = static_cast<unsigned *>(ws.ptr);
+    a.D = reinterpret_cast<float *>(static_cast<uint8_t *>(ws.ptr) + 256);
+    a.heads_per_group = heads_per_group(B, H, T, d, dtype);
     a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)d));
     a.dq = dq;
     a.dk = dk;

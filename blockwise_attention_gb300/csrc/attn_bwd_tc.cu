@@ -42,13 +42,28 @@ struct BCfg {
     static constexpr int VEC_OFF = 2 * TILE_BYTES;        // within a stage: 128 LSE (log2 units) + 128 D
     static constexpr int STG_BYTES = 2 * TILE_BYTES + 1024;
     static constexpr int BAR_OFF = STG_OFF + NST * STG_BYTES;
-    // S_FULL[h], P_FULL[h]: half h (64 query / key columns) of the tile's scores and products
-    enum { B_RES = 0, B_FULL, B_EMPTY = B_FULL + NST, B_SFULL = B_EMPTY + NST, B_PFULL = B_SFULL + 2, B_DONE = B_PFULL + 2,
-           B_DRAIN, NBAR };
-    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort
+    // RES_FULL / RES_EMPTY: the resident pair of the current item loaded / no longer read.
+    // S_FULL[h], P_FULL[h]: half h (64 query / key columns) of the tile's scores and products.
+    // ACC_FULL / ACC_EMPTY: the item's accumulators complete / read out by the epilogue.
+    // ITEM_FULL[s] / ITEM_EMPTY[s]: the two-slot ring of claimed items.
+    enum {
+        B_RES = 0,
+        B_RESE,
+        B_FULL,
+        B_EMPTY = B_FULL + NST,
+        B_SFULL = B_EMPTY + NST,
+        B_PFULL = B_SFULL + 2,
+        B_ACCF = B_PFULL + 2,
+        B_ACCE,
+        B_DRAIN,
+        B_ITEMF,
+        B_ITEME = B_ITEMF + 2,
+        NBAR = B_ITEME + 2
+    };
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // [0] tmem base, [1] abort, [4..5] item by slot
     // At least 120 KB, so that one CTA occupies an SM: each CTA allocates all
     // 512 TMEM columns, and a second one would wait inside tcgen05.alloc.
-    static constexpr int SMEM_USED = MISC_OFF + 16 + 1024;
+    static constexpr int SMEM_USED = MISC_OFF + 32 + 1024;   // misc words [0..5], + slack to align the base to 1 KB
     static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static constexpr uint32_t S_COL = 0, DP_COL = 128, ACC0_COL = 256, ACC1_COL = 256 + D;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -93,6 +108,21 @@ __device__ __forceinline__ BTile btile(const BwdArgs &a, int t, bool is_q) {
 __device__ __forceinline__ int n_tiles_side(const BwdArgs &a, bool is_q) {
     if (a.ring) return a.NC * ((a.CL + TILE - 1) / TILE);
     return ((is_q ? a.Lq : a.Lk) + TILE - 1) / TILE;
+}
+
+// Work item w of a persistent backward kernel -> (own tile, b * H + h).  Items are
+// grouped by heads_per_group (b, h) pairs so that concurrently running CTAs share
+// the streamed side in L2; within a group they come heaviest first under causal
+// masking: the earliest key tiles (dK/dV: every later query sees them), the latest
+// query tiles (dQ: they see every earlier key).
+__device__ __forceinline__ void bwd_item(const BwdArgs &a, int w, int n_side, bool own_is_q, int &tile, int &bh) {
+    const int BH = a.B * a.H, G = a.heads_per_group > 0 ? a.heads_per_group : 1;
+    const int per_group = G * n_side;
+    const int grp = w / per_group, rem = w % per_group;
+    const int g_heads = BH - grp * G < G ? BH - grp * G : G;   // last group may be short
+    const int lvl = rem / g_heads;
+    bh = grp * G + rem % g_heads;
+    tile = own_is_q ? n_side - 1 - lvl : lvl;
 }
 
 // Walk over the partner tiles of an own tile: the rows of the other side that
@@ -224,6 +254,7 @@ __device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     if (threadIdx.x == 0) {
         mbar_init(bar(C::B_RES), 1);
+        mbar_init(bar(C::B_RESE), 1);
         for (int i = 0; i < C::NST; ++i) {
             mbar_init(bar(C::B_FULL + i), full_count);
             mbar_init(bar(C::B_EMPTY + i), 1);
@@ -232,8 +263,13 @@ __device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_
             mbar_init(bar(C::B_SFULL + hh), 1);
             mbar_init(bar(C::B_PFULL + hh), 128);
         }
-        mbar_init(bar(C::B_DONE), 1);
+        mbar_init(bar(C::B_ACCF), 1);
+        mbar_init(bar(C::B_ACCE), 128);   // every elementwise thread after its epilogue
         mbar_init(bar(C::B_DRAIN), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_ITEMF + i), 1);
+            mbar_init(bar(C::B_ITEME + i), 1 + 4);   // MMA warp + one lane per elementwise warp
+        }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -317,58 +353,92 @@ __global__ void __launch_bounds__(256, 1)
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
-    const BTile kt = btile(a, blockIdx.x, false);
     const long long q_rows = a.ring ? a.T : a.Lq;
+    const int n_side = n_tiles_side(a, false), n_items = n_side * a.B * a.H;
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t tmem = bwd_prologue<D>(bars, misc, base + C::MISC_OFF, 32, &tq, &tk, &tv, &tdo);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (all lanes)
+        // Claims key tiles (items) from the launch's counter, publishes them, loads the
+        // item's resident K / V once the previous item's score products are done with
+        // them, then streams the query tiles of its walk (Q, dout, and the rows' LSE / D).
         bool ok = true;
-        uint32_t fills = 0;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
-            tma_tile<D>(sK, &tk, kt.row0, h, b, bar(C::B_RES));
-            tma_tile<D>(sV, &tv, kt.row0, h, b, bar(C::B_RES));
-        }
-        PWalk pw;
-        pwalk_begin(a, kt, true, pw);
-        BTile pt;
-        while (ok && pwalk_next(a, kt, true, pw, pt)) {
-            const int st = fills % C::NST;
-            const uint32_t use = fills / C::NST;
-            if (use > 0 && !warp_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+        uint32_t fills = 0, loads = 0;
+        int w = 0;
+        if (lane == 0) w = (int)atomicAdd(a.sched, 1u);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t sl = it & 1;
+            if (it >= 2 && !warp_wait(bar(C::B_ITEME + sl), ((it >> 1) - 1) & 1, abort, a.err, lim)) {
                 ok = false;
                 break;
             }
-            float *lse2 = vec(st), *dd = lse2 + TILE;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = lane * 4 + i;
-                float L = -INFINITY, Dv = 0.f;
-                if (c < pt.len) {
-                    const long long row = (long long)bh * q_rows + pt.row0 + c;
-                    L = a.lse[row];
-                    Dv = a.D[row];
-                }
-                // -LSE in log2 units; -inf makes p = exp2(x + nlse2) exactly 0 for rows
-                // past the tile and rows without keys
-                lse2[c] = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
-                dd[c] = Dv;
+            if (w >= n_items) {
+                if (lane == 0) misc[4 + sl] = 0xffffffffu;   // end of work
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_ITEMF + sl));
+                break;
+            }
+            int ktile, bh;
+            bwd_item(a, w, n_side, false, ktile, bh);
+            const int b = bh / a.H, h = bh % a.H;
+            const BTile kt = btile(a, ktile, false);
+            if (lane == 0) misc[4 + sl] = (uint32_t)w;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEMF + sl));
+            if (it > 0 && !warp_wait(bar(C::B_RESE), (it - 1) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
-                tma_tile<D>(stage(st), &tq, pt.row0, h, b, bar(C::B_FULL + st));
-                tma_tile<D>(stage(st) + C::TILE_BYTES, &tdo, pt.row0, h, b, bar(C::B_FULL + st));
-            } else {
-                mbar_arrive(bar(C::B_FULL + st));
+                mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
+                tma_tile<D>(sK, &tk, kt.row0, h, b, bar(C::B_RES));
+                tma_tile<D>(sV, &tv, kt.row0, h, b, bar(C::B_RES));
             }
-            ++fills;
+            ++loads;
+            PWalk pw;
+            pwalk_begin(a, kt, true, pw);
+            BTile pt;
+            while (ok && pwalk_next(a, kt, true, pw, pt)) {
+                const int st = fills % C::NST;
+                const uint32_t use = fills / C::NST;
+                if (use > 0 && !warp_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                float *lse2 = vec(st), *dd = lse2 + TILE;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = lane * 4 + i;
+                    float L = -INFINITY, Dv = 0.f;
+                    if (c < pt.len) {
+                        const long long row = (long long)bh * q_rows + pt.row0 + c;
+                        L = a.lse[row];
+                        Dv = a.D[row];
+                    }
+                    // -LSE in log2 units; -inf makes p = exp2(x + nlse2) exactly 0 for rows
+                    // past the tile and rows without keys
+                    lse2[c] = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
+                    dd[c] = Dv;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+                    tma_tile<D>(stage(st), &tq, pt.row0, h, b, bar(C::B_FULL + st));
+                    tma_tile<D>(stage(st) + C::TILE_BYTES, &tdo, pt.row0, h, b, bar(C::B_FULL + st));
+                } else {
+                    mbar_arrive(bar(C::B_FULL + st));
+                }
+                ++fills;
+            }
+            if (!ok) break;
+            if (lane == 0) w = (int)atomicAdd(a.sched, 1u);
+            w = __shfl_sync(0xffffffffu, w, 0);
         }
         if (!ok && lane == 0) {
+            // Let the copies already issued land before the CTA exits.
             volatile int never = 0;
-            mbar_wait(bar(C::B_RES), 0, &never, nullptr, 200000000ull);
+            if (loads > 0) mbar_wait(bar(C::B_RES), (loads - 1) & 1, &never, nullptr, 200000000ull);
             for (uint32_t i = 0; i < (uint32_t)C::NST && i < fills; ++i) {
                 const uint32_t last = fills - 1 - i;
                 mbar_wait(bar(C::B_FULL + last % C::NST), (last / C::NST) & 1, &never, nullptr, 200000000ull);
@@ -384,7 +454,11 @@ __global__ void __launch_bounds__(256, 1)
         // warps work on the other.  Half h of S^T / dP^T lives in columns
         // [64 h, 64 h + 64) of its region and its bf16 P^T / dS^T in the first 32 of
         // them, so the next tile's half 0 never touches what half 1 still needs.
-        bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
+        // Across items: RES_EMPTY is committed after an item's last score products
+        // (the producer may then load the next item's K / V), ACC_FULL after its last
+        // gradient products, and an item's first gradient products wait for ACC_EMPTY
+        // of the previous one (its epilogue has read the accumulators).
+        bool ok = true;
         const uint64_t kdesc = sdesc(sK, 16, 1024), vdesc = sdesc(sV, 16, 1024);   // K-major A operands
         // S^T_h = K Q_h^T and dP^T_h = V dout_h^T (fp32 into TMEM) for the tile in stage st
         auto scores = [&](int st, int hh) {
@@ -420,36 +494,60 @@ __global__ void __launch_bounds__(256, 1)
                            (first && kk == 0) ? 0u : 1u);   // dK += dS^T q
             return true;
         };
-        uint32_t t = 0;
-        PWalk pw;
-        pwalk_begin(a, kt, true, pw);
-        BTile pt;
-        bool have = ok && pwalk_next(a, kt, true, pw, pt);
-        if (have) {
-            if (!warp_wait(bar(C::B_FULL), 0, abort, a.err, lim)) {
+        uint32_t t = 0;   // query tiles so far, over all items (stage and barrier phases)
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t sl = it & 1;
+            if (!warp_wait(bar(C::B_ITEMF + sl), (it >> 1) & 1, abort, a.err, lim)) {
                 ok = false;
-            } else {
-                scores(0, 0);
-                scores(0, 1);
+                break;
             }
-        }
-        while (ok && have) {
-            const int st = t % C::NST, stn = (t + 1) % C::NST;
-            const bool more = pwalk_next(a, kt, true, pw, pt);
-            if (!(ok = grads(st, 0, t, t == 0))) break;
-            if (more) {
-                if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
-                scores(stn, 0);
+            const uint32_t w = misc[4 + sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEME + sl));
+            if (w == 0xffffffffu) break;
+            int ktile, bh;
+            bwd_item(a, (int)w, n_side, false, ktile, bh);
+            const BTile kt = btile(a, ktile, false);
+            if (!warp_wait(bar(C::B_RES), it & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
             }
-            if (!(ok = grads(st, 1, t, false))) break;
-            mma_commit_one(bar(C::B_EMPTY + st));
-            if (more) scores(stn, 1);
-            ++t;
-            have = more;
+            PWalk pw;
+            pwalk_begin(a, kt, true, pw);
+            BTile pt;
+            bool have = pwalk_next(a, kt, true, pw, pt);
+            if (!have) {
+                // no query sees this key tile: the accumulators are not touched
+                mma_commit_one(bar(C::B_RESE));
+                if (it > 0 && !(ok = warp_wait(bar(C::B_ACCE), (it - 1) & 1, abort, a.err, lim))) break;
+                mma_commit_one(bar(C::B_ACCF));
+                continue;
+            }
+            if (!(ok = warp_wait(bar(C::B_FULL + t % C::NST), (t / C::NST) & 1, abort, a.err, lim))) break;
+            scores(t % C::NST, 0);
+            scores(t % C::NST, 1);
+            bool first = true;
+            while (have) {
+                const int st = t % C::NST, stn = (t + 1) % C::NST;
+                const bool more = pwalk_next(a, kt, true, pw, pt);
+                if (!more) mma_commit_one(bar(C::B_RESE));   // the item's last score products are issued
+                if (first && it > 0 && !(ok = warp_wait(bar(C::B_ACCE), (it - 1) & 1, abort, a.err, lim))) break;
+                if (!(ok = grads(st, 0, t, first))) break;
+                first = false;
+                if (more) {
+                    if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
+                    scores(stn, 0);
+                }
+                if (!(ok = grads(st, 1, t, false))) break;
+                mma_commit_one(bar(C::B_EMPTY + st));
+                if (more) scores(stn, 1);
+                ++t;
+                have = more;
+            }
+            if (!ok) break;
+            mma_commit_one(bar(C::B_ACCF));
         }
-        if (ok) {
-            mma_commit_one(bar(C::B_DONE));
-        } else {
+        if (!ok) {
             volatile int never = 0;
             mma_commit_one(bar(C::B_DRAIN));
             warp_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
@@ -459,81 +557,102 @@ __global__ void __launch_bounds__(256, 1)
         // ------------------------------------------------------------ elementwise + epilogue
         const int j = (warp & 3) * 32 + lane;               // key row of the tile (TMEM lane)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const bool jvalid = j < kt.len;
-        const long long kp = kt.pos0 + j;
         const float sl2 = a.scale * 1.4426950408889634f;
         bool ok = true;
-        uint32_t t = 0;
-        PWalk pw;
-        pwalk_begin(a, kt, true, pw);
-        BTile pt;
-        while (ok && pwalk_next(a, kt, true, pw, pt)) {
-            const int st = t % C::NST;
-            const uint32_t s_nlse = smem_u32(vec(st)), s_dd = s_nlse + TILE * 4;   // -LSE log2 units, D
-            const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
-                              (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
-            // Not unrolled: four copies of this body did not fit the instruction cache
-            // (ncu: warps stalled mostly on instruction fetch).
+        uint32_t t = 0;   // query tiles so far, over all items
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t sl = it & 1;
+            if (!warp_wait(bar(C::B_ITEMF + sl), (it >> 1) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t w = misc[4 + sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEME + sl));
+            if (w == 0xffffffffu) break;
+            int ktile, bh;
+            bwd_item(a, (int)w, n_side, false, ktile, bh);
+            const int b = bh / a.H;
+            const BTile kt = btile(a, ktile, false);
+            const bool jvalid = j < kt.len;
+            const long long kp = kt.pos0 + j;
+            uint32_t n_done = 0;   // query tiles of this item (the same for every lane)
+            PWalk pw;
+            pwalk_begin(a, kt, true, pw);
+            BTile pt;
+            while (ok && pwalk_next(a, kt, true, pw, pt)) {
+                const int st = t % C::NST;
+                const uint32_t s_nlse = smem_u32(vec(st)), s_dd = s_nlse + TILE * 4;   // -LSE log2 units, D
+                const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
+                                  (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
 #pragma unroll 1
-            for (int c = 0; c < TILE / 32; ++c) {
-                const int hh = c >> 1;   // half of the tile: queries [64 hh, 64 hh + 64)
-                if ((c & 1) == 0) {
-                    if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
+                for (int c = 0; c < TILE / 32; ++c) {
+                    const int hh = c >> 1;   // half of the tile: queries [64 hh, 64 hh + 64)
+                    if ((c & 1) == 0) {
+                        if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                }
-                uint32_t rs[32], rd[32];
-                tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
-                tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
-                tmem_wait_ld();
-                const uint32_t keep =
-                    full ? 0xffffffffu
-                         : keep_bits_queries(a, b, pt.pos0 + c * 32, pt.len - c * 32, kp, jvalid);
-                uint32_t pp[16], pd[16];
+                    uint32_t rs[32], rd[32];
+                    tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
+                    tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
+                    tmem_wait_ld();
+                    const uint32_t keep =
+                        full ? 0xffffffffu
+                             : keep_bits_queries(a, b, pt.pos0 + c * 32, pt.len - c * 32, kp, jvalid);
+                    uint32_t pp[16], pd[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 nl = lds4(s_nlse + (c * 32 + q4 * 4) * 4);
-                    const float4 d4 = lds4(s_dd + (c * 32 + q4 * 4) * 4);
-                    const float nlv[4] = {nl.x, nl.y, nl.z, nl.w}, ddv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dv[4];
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 nl = lds4(s_nlse + (c * 32 + q4 * 4) * 4);
+                        const float4 d4 = lds4(s_dd + (c * 32 + q4 * 4) * 4);
+                        const float nlv[4] = {nl.x, nl.y, nl.z, nl.w}, ddv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pv[4], dv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = q4 * 4 + e;
-                        float p = fast_exp2(fmaf(__uint_as_float(rs[i]), sl2, nlv[e]));
-                        p = (keep >> i) & 1u ? p : 0.f;   // columns past the partner tile are never kept
-                        pv[e] = p;
-                        dv[e] = p * (__uint_as_float(rd[i]) - ddv[e]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = q4 * 4 + e;
+                            float p = fast_exp2(fmaf(__uint_as_float(rs[i]), sl2, nlv[e]));
+                            p = (keep >> i) & 1u ? p : 0.f;   // columns past the partner tile are never kept
+                            pv[e] = p;
+                            dv[e] = p * (__uint_as_float(rd[i]) - ddv[e]);
+                        }
+                        pp[q4 * 2] = pack_bf16(pv[0], pv[1]);
+                        pp[q4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
+                        pd[q4 * 2] = pack_bf16(dv[0], dv[1]);
+                        pd[q4 * 2 + 1] = pack_bf16(dv[2], dv[3]);
                     }
-                    pp[q4 * 2] = pack_bf16(pv[0], pv[1]);
-                    pp[q4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
-                    pd[q4 * 2] = pack_bf16(dv[0], dv[1]);
-                    pd[q4 * 2 + 1] = pack_bf16(dv[2], dv[3]);
+                    // P^T / dS^T of these 32 queries into 16 columns of this half that the
+                    // earlier chunk of the half has read
+                    const uint32_t pcol = hh * C::HALF + (c & 1) * 16;
+                    tmem_st16(tmem + lane_addr + C::S_COL + pcol, pp);
+                    tmem_st16(tmem + lane_addr + C::DP_COL + pcol, pd);
+                    if (c & 1) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(bar(C::B_PFULL + hh));
+                    }
                 }
-                // P^T / dS^T of these 32 queries into 16 columns of this half that the
-                // earlier chunk of the half has read
-                const uint32_t pcol = hh * C::HALF + (c & 1) * 16;
-                tmem_st16(tmem + lane_addr + C::S_COL + pcol, pp);
-                tmem_st16(tmem + lane_addr + C::DP_COL + pcol, pd);
-                if (c & 1) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_PFULL + hh));
-                }
+                if (!ok) break;
+                ++t;
+                ++n_done;
             }
             if (!ok) break;
-            ++t;
-        }
-        if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {
+            // epilogue of the item: the accumulators to dV / dK rows, then hand them back
+            if (!warp_wait(bar(C::B_ACCF), it & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const long long row = ((long long)bh * (a.ring ? a.T : a.Lk) + kt.row0 + j) * D;
-            if (t > 0) {   // t is the same for every lane: the TMEM loads below stay warp-collective
+            if (n_done > 0) {   // the same for every lane: the TMEM loads below stay warp-collective
                 store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dv + row, 1.f, a.accumulate != 0, jvalid);
                 store_acc_row<D>(tmem + lane_addr + C::ACC1_COL, a.dk + row, a.scale, a.accumulate != 0, jvalid);
             } else if (jvalid && !a.accumulate) {
                 for (int c = 0; c < D; ++c) a.dv[row + c] = a.dk[row + c] = 0.f;
             }
+            tc_fence_before();
+            mbar_arrive(bar(C::B_ACCE));
         }
     }
 
@@ -566,39 +685,67 @@ __global__ void __launch_bounds__(256, 1)
     auto stage = [&](int st) { return base + C::STG_OFF + (uint32_t)st * C::STG_BYTES; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
-    // heaviest query tiles first under causal masking (the last tiles see the most keys)
-    const BTile qt = btile(a, n_tiles_side(a, true) - 1 - (int)blockIdx.x, true);
     const long long q_rows = a.ring ? a.T : a.Lq;
+    const int n_side = n_tiles_side(a, true), n_items = n_side * a.B * a.H;
     const uint64_t lim = a.wait_limit_ns;
     const uint32_t tmem = bwd_prologue<D>(bars, misc, base + C::MISC_OFF, 1, &tq, &tk, &tv, &tdo);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (one lane)
+        // Claims query tiles (items), publishes them, loads the item's resident Q / dout
+        // once the previous item's score products are done with them, then streams the
+        // K / V tiles of its walk.
         if (lane == 0) {
             bool ok = true;
-            uint32_t fills = 0;
-            mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
-            tma_tile<D>(sQ, &tq, qt.row0, h, b, bar(C::B_RES));
-            tma_tile<D>(sDO, &tdo, qt.row0, h, b, bar(C::B_RES));
-            PWalk pw;
-            pwalk_begin(a, qt, false, pw);
-            BTile pt;
-            while (pwalk_next(a, qt, false, pw, pt)) {
-                const int st = fills % C::NST;
-                const uint32_t use = fills / C::NST;
-                if (use > 0 && !mbar_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+            uint32_t fills = 0, loads = 0;
+            int w = (int)atomicAdd(a.sched + 1, 1u);
+            for (uint32_t it = 0;; ++it) {
+                const uint32_t sl = it & 1;
+                if (it >= 2 && !mbar_wait(bar(C::B_ITEME + sl), ((it >> 1) - 1) & 1, abort, a.err, lim)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
-                tma_tile<D>(stage(st), &tk, pt.row0, h, b, bar(C::B_FULL + st));
-                tma_tile<D>(stage(st) + C::TILE_BYTES, &tv, pt.row0, h, b, bar(C::B_FULL + st));
-                ++fills;
+                if (w >= n_items) {
+                    misc[4 + sl] = 0xffffffffu;   // end of work
+                    mbar_arrive(bar(C::B_ITEMF + sl));
+                    break;
+                }
+                int qtile, bh;
+                bwd_item(a, w, n_side, true, qtile, bh);
+                const int b = bh / a.H, h = bh % a.H;
+                const BTile qt = btile(a, qtile, true);
+                misc[4 + sl] = (uint32_t)w;
+                mbar_arrive(bar(C::B_ITEMF + sl));
+                if (it > 0 && !mbar_wait(bar(C::B_RESE), (it - 1) & 1, abort, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(C::B_RES), 2 * C::TILE_BYTES);
+                tma_tile<D>(sQ, &tq, qt.row0, h, b, bar(C::B_RES));
+                tma_tile<D>(sDO, &tdo, qt.row0, h, b, bar(C::B_RES));
+                ++loads;
+                PWalk pw;
+                pwalk_begin(a, qt, false, pw);
+                BTile pt;
+                while (pwalk_next(a, qt, false, pw, pt)) {
+                    const int st = fills % C::NST;
+                    const uint32_t use = fills / C::NST;
+                    if (use > 0 && !mbar_wait(bar(C::B_EMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::B_FULL + st), 2 * C::TILE_BYTES);
+                    tma_tile<D>(stage(st), &tk, pt.row0, h, b, bar(C::B_FULL + st));
+                    tma_tile<D>(stage(st) + C::TILE_BYTES, &tv, pt.row0, h, b, bar(C::B_FULL + st));
+                    ++fills;
+                }
+                if (!ok) break;
+                w = (int)atomicAdd(a.sched + 1, 1u);
             }
             if (!ok) {
+                // Let the copies already issued land before the CTA exits.
                 volatile int never = 0;
-                mbar_wait(bar(C::B_RES), 0, &never, nullptr, 200000000ull);
+                if (loads > 0) mbar_wait(bar(C::B_RES), (loads - 1) & 1, &never, nullptr, 200000000ull);
                 for (uint32_t i = 0; i < (uint32_t)C::NST && i < fills; ++i) {
                     const uint32_t last = fills - 1 - i;
                     mbar_wait(bar(C::B_FULL + last % C::NST), (last / C::NST) & 1, &never, nullptr, 200000000ull);
@@ -611,8 +758,9 @@ __global__ void __launch_bounds__(256, 1)
         // Each key tile is taken in two halves of 64 keys, in the order of the dK/dV
         // kernel: dQ += half 0, the next tile's half-0 scores, dQ += half 1, the next
         // tile's half-1 scores.  Half h of S / dP lives in columns [64 h, 64 h + 64)
-        // of its region and its bf16 dS in the first 32 of them.
-        bool ok = warp_wait(bar(C::B_RES), 0, abort, a.err, lim);
+        // of its region and its bf16 dS in the first 32 of them.  Across items as in
+        // the dK/dV kernel (RES_EMPTY, ACC_FULL, ACC_EMPTY).
+        bool ok = true;
         const uint64_t qdesc = sdesc(sQ, 16, 1024), dodesc = sdesc(sDO, 16, 1024);   // K-major A operands
         // S_h = Q K_h^T and dP_h = dout V_h^T for the tile in stage st
         auto scores = [&](int st, int hh) {
@@ -642,36 +790,59 @@ __global__ void __launch_bounds__(256, 1)
                            (first && kk == 0) ? 0u : 1u);   // dQ += dS K
             return true;
         };
-        uint32_t t = 0;
-        PWalk pw;
-        pwalk_begin(a, qt, false, pw);
-        BTile pt;
-        bool have = ok && pwalk_next(a, qt, false, pw, pt);
-        if (have) {
-            if (!warp_wait(bar(C::B_FULL), 0, abort, a.err, lim)) {
+        uint32_t t = 0;   // key tiles so far, over all items
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t sl = it & 1;
+            if (!warp_wait(bar(C::B_ITEMF + sl), (it >> 1) & 1, abort, a.err, lim)) {
                 ok = false;
-            } else {
-                scores(0, 0);
-                scores(0, 1);
+                break;
             }
-        }
-        while (ok && have) {
-            const int st = t % C::NST, stn = (t + 1) % C::NST;
-            const bool more = pwalk_next(a, qt, false, pw, pt);
-            if (!(ok = grads(st, 0, t, t == 0))) break;
-            if (more) {
-                if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
-                scores(stn, 0);
+            const uint32_t w = misc[4 + sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEME + sl));
+            if (w == 0xffffffffu) break;
+            int qtile, bh;
+            bwd_item(a, (int)w, n_side, true, qtile, bh);
+            const BTile qt = btile(a, qtile, true);
+            if (!warp_wait(bar(C::B_RES), it & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
             }
-            if (!(ok = grads(st, 1, t, false))) break;
-            mma_commit_one(bar(C::B_EMPTY + st));
-            if (more) scores(stn, 1);
-            ++t;
-            have = more;
+            PWalk pw;
+            pwalk_begin(a, qt, false, pw);
+            BTile pt;
+            bool have = pwalk_next(a, qt, false, pw, pt);
+            if (!have) {
+                mma_commit_one(bar(C::B_RESE));
+                if (it > 0 && !(ok = warp_wait(bar(C::B_ACCE), (it - 1) & 1, abort, a.err, lim))) break;
+                mma_commit_one(bar(C::B_ACCF));
+                continue;
+            }
+            if (!(ok = warp_wait(bar(C::B_FULL + t % C::NST), (t / C::NST) & 1, abort, a.err, lim))) break;
+            scores(t % C::NST, 0);
+            scores(t % C::NST, 1);
+            bool first = true;
+            while (have) {
+                const int st = t % C::NST, stn = (t + 1) % C::NST;
+                const bool more = pwalk_next(a, qt, false, pw, pt);
+                if (!more) mma_commit_one(bar(C::B_RESE));   // the item's last score products are issued
+                if (first && it > 0 && !(ok = warp_wait(bar(C::B_ACCE), (it - 1) & 1, abort, a.err, lim))) break;
+                if (!(ok = grads(st, 0, t, first))) break;
+                first = false;
+                if (more) {
+                    if (!(ok = warp_wait(bar(C::B_FULL + stn), ((t + 1) / C::NST) & 1, abort, a.err, lim))) break;
+                    scores(stn, 0);
+                }
+                if (!(ok = grads(st, 1, t, false))) break;
+                mma_commit_one(bar(C::B_EMPTY + st));
+                if (more) scores(stn, 1);
+                ++t;
+                have = more;
+            }
+            if (!ok) break;
+            mma_commit_one(bar(C::B_ACCF));
         }
-        if (ok) {
-            mma_commit_one(bar(C::B_DONE));
-        } else {
+        if (!ok) {
             volatile int never = 0;
             mma_commit_one(bar(C::B_DRAIN));
             warp_wait(bar(C::B_DRAIN), 0, &never, nullptr, 200000000ull);
@@ -681,73 +852,95 @@ __global__ void __launch_bounds__(256, 1)
         // ------------------------------------------------------------ elementwise + epilogue
         const int i = (warp & 3) * 32 + lane;               // query row of the tile (TMEM lane)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const bool ivalid = i < qt.len;
-        const long long qp = qt.pos0 + i;
         const float sl2 = a.scale * 1.4426950408889634f;
-        float nlse2 = -INFINITY, Dv = 0.f;   // -LSE in log2 units (-inf: p = 0)
-        if (ivalid) {
-            const long long row = (long long)bh * q_rows + qt.row0 + i;
-            const float L = a.lse[row];
-            nlse2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
-            Dv = a.D[row];
-        }
         bool ok = true;
-        uint32_t t = 0;
-        PWalk pw;
-        pwalk_begin(a, qt, false, pw);
-        BTile pt;
-        while (ok && pwalk_next(a, qt, false, pw, pt)) {
-            const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
-                              (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
-            // Not unrolled, as in the dK/dV kernel (instruction cache).
+        uint32_t t = 0;   // key tiles so far, over all items
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t sl = it & 1;
+            if (!warp_wait(bar(C::B_ITEMF + sl), (it >> 1) & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
+            const uint32_t w = misc[4 + sl];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ITEME + sl));
+            if (w == 0xffffffffu) break;
+            int qtile, bh;
+            bwd_item(a, (int)w, n_side, true, qtile, bh);
+            const int b = bh / a.H;
+            const BTile qt = btile(a, qtile, true);
+            const bool ivalid = i < qt.len;
+            const long long qp = qt.pos0 + i;
+            float nlse2 = -INFINITY, Dv = 0.f;   // -LSE in log2 units (-inf: p = 0)
+            if (ivalid) {
+                const long long row = (long long)bh * q_rows + qt.row0 + i;
+                const float L = a.lse[row];
+                nlse2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
+                Dv = a.D[row];
+            }
+            uint32_t n_done = 0;   // key tiles of this item (the same for every lane)
+            PWalk pw;
+            pwalk_begin(a, qt, false, pw);
+            BTile pt;
+            while (ok && pwalk_next(a, qt, false, pw, pt)) {
+                const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
+                                  (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
 #pragma unroll 1
-            for (int c = 0; c < TILE / 32; ++c) {
-                const int hh = c >> 1;   // half of the tile: keys [64 hh, 64 hh + 64)
-                if ((c & 1) == 0) {
-                    if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
-                        ok = false;
-                        break;
+                for (int c = 0; c < TILE / 32; ++c) {
+                    const int hh = c >> 1;   // half of the tile: keys [64 hh, 64 hh + 64)
+                    if ((c & 1) == 0) {
+                        if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                }
-                uint32_t rs[32], rd[32];
-                tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
-                tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
-                tmem_wait_ld();
-                const uint32_t keep =
-                    full ? 0xffffffffu : keep_bits_keys(a, b, qp, ivalid, pt.pos0 + c * 32, pt.len - c * 32);
-                uint32_t pd[16];
+                    uint32_t rs[32], rd[32];
+                    tmem_ld32(tmem + lane_addr + C::S_COL + c * 32, rs);
+                    tmem_ld32(tmem + lane_addr + C::DP_COL + c * 32, rd);
+                    tmem_wait_ld();
+                    const uint32_t keep =
+                        full ? 0xffffffffu : keep_bits_keys(a, b, qp, ivalid, pt.pos0 + c * 32, pt.len - c * 32);
+                    uint32_t pd[16];
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2) {
-                    float dv[2];
+                    for (int k2 = 0; k2 < 16; ++k2) {
+                        float dv[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = 2 * k2 + e;
-                        float p = fast_exp2(fmaf(__uint_as_float(rs[k]), sl2, nlse2));
-                        p = (keep >> k) & 1u ? p : 0.f;
-                        dv[e] = p * (__uint_as_float(rd[k]) - Dv);
+                        for (int e = 0; e < 2; ++e) {
+                            const int k = 2 * k2 + e;
+                            float p = fast_exp2(fmaf(__uint_as_float(rs[k]), sl2, nlse2));
+                            p = (keep >> k) & 1u ? p : 0.f;
+                            dv[e] = p * (__uint_as_float(rd[k]) - Dv);
+                        }
+                        pd[k2] = pack_bf16(dv[0], dv[1]);
                     }
-                    pd[k2] = pack_bf16(dv[0], dv[1]);
+                    // dS of these 32 keys into 16 columns of this half that the earlier
+                    // chunk of the half has read
+                    tmem_st16(tmem + lane_addr + C::S_COL + hh * C::HALF + (c & 1) * 16, pd);
+                    if (c & 1) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(bar(C::B_PFULL + hh));
+                    }
                 }
-                // dS of these 32 keys into 16 columns of this half that the earlier
-                // chunk of the half has read
-                tmem_st16(tmem + lane_addr + C::S_COL + hh * C::HALF + (c & 1) * 16, pd);
-                if (c & 1) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(bar(C::B_PFULL + hh));
-                }
+                if (!ok) break;
+                ++t;
+                ++n_done;
             }
             if (!ok) break;
-            ++t;
-        }
-        if (ok && warp_wait(bar(C::B_DONE), 0, abort, a.err, lim)) {
+            // epilogue of the item: the accumulator to dQ rows, then hand it back
+            if (!warp_wait(bar(C::B_ACCF), it & 1, abort, a.err, lim)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const long long row = ((long long)bh * q_rows + qt.row0 + i) * D;
-            if (t > 0)   // uniform: the TMEM loads stay warp-collective
+            if (n_done > 0)   // uniform: the TMEM loads stay warp-collective
                 store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dq + row, a.scale, a.accumulate != 0, ivalid);
             else if (ivalid && !a.accumulate)
                 for (int c = 0; c < D; ++c) a.dq[row + c] = 0.f;
+            tc_fence_before();
+            mbar_arrive(bar(C::B_ACCE));
         }
     }
 
@@ -760,7 +953,7 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int D>
-int launch_bwd_tc_d(const BwdArgs &a, const BwdMaps &m, cudaStream_t s) {
+int launch_bwd_tc_d(const BwdArgs &a, const BwdMaps &m, int num_sms, cudaStream_t s) {
     using C = BCfg<D>;
     static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
     if (cudaFuncSetAttribute(bwd_dkdv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
@@ -768,11 +961,21 @@ int launch_bwd_tc_d(const BwdArgs &a, const BwdMaps &m, cudaStream_t s) {
         cudaFuncSetAttribute(bwd_dq_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
             cudaSuccess)
         return BA_ERR_CUDA;
-    const int BH = a.B * a.H;
-    const int n_kt = a.ring ? a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lk + TILE - 1) / TILE;
-    const int n_qt = a.ring ? a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lq + TILE - 1) / TILE;
-    if (n_kt > 0) bwd_dkdv_tc_kernel<D><<<dim3(n_kt, BH), 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
-    if (n_qt > 0) bwd_dq_tc_kernel<D><<<dim3(n_qt, BH), 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    // CTAs claim (own tile, b, h) items from a zeroed counter, heaviest first.  Short
+    // walks (fewer than 256 tiles per head): one persistent CTA per SM, the next item's
+    // first score products overlapping the previous item's epilogue.  Long walks: one
+    // CTA per item (each claims one and exits), which measured faster there.
+    if (cudaMemsetAsync(a.sched, 0, 2 * sizeof(unsigned), s) != cudaSuccess) return BA_ERR_CUDA;
+    const long long BH = (long long)a.B * a.H;
+    const long long n_kt = a.ring ? (long long)a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lk + TILE - 1) / TILE;
+    const long long n_qt = a.ring ? (long long)a.NC * ((a.CL + TILE - 1) / TILE) : (a.Lq + TILE - 1) / TILE;
+    if (n_kt * BH > 0x7fffffffLL || n_qt * BH > 0x7fffffffLL) return BA_ERR_SHAPE;
+    const bool persistent = n_kt < 256 && n_qt < 256;
+    const long long cap = persistent ? num_sms : 0x7fffffffLL;
+    const int g_kv = (int)(n_kt * BH < cap ? n_kt * BH : cap);
+    const int g_q = (int)(n_qt * BH < cap ? n_qt * BH : cap);
+    if (g_kv > 0) bwd_dkdv_tc_kernel<D><<<g_kv, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    if (g_q > 0) bwd_dq_tc_kernel<D><<<g_q, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -782,13 +985,11 @@ bool bwd_tc_supported(int dtype, int d) { return dtype == BA_BF16 && (d == 64 ||
 
 // D pre-pass, then the dK/dV and dQ tensor-core kernels.
 int launch_attn_bwd_tc(const BwdArgs &a, const BwdMaps &m, int num_sms, cudaStream_t s) {
-    const int BH = a.B * a.H;
-    if (BH == 0) return BA_OK;
-    if (BH > 65535) return BA_ERR_SHAPE;
+    if ((long long)a.B * a.H == 0) return BA_OK;
     int rc = launch_bwd_pre(a, num_sms, s);
     if (rc) return rc;
-    if (a.d == 128) return launch_bwd_tc_d<128>(a, m, s);
-    if (a.d == 64) return launch_bwd_tc_d<64>(a, m, s);
+    if (a.d == 128) return launch_bwd_tc_d<128>(a, m, num_sms, s);
+    if (a.d == 64) return launch_bwd_tc_d<64>(a, m, num_sms, s);
     return BA_ERR_SHAPE;
 }
 

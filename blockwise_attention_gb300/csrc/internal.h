@@ -57,6 +57,8 @@ struct BwdArgs {
     int accumulate;                      // add into dq / dk / dv instead of overwriting
     unsigned *err;                       // device error word (tensor-core kernels)
     unsigned long long wait_limit_ns;    // bounded-wait limit (tensor-core kernels)
+    unsigned *sched;                     // 2 zeroed item counters (dK/dV kernel, dQ kernel), tensor-core kernels
+    int heads_per_group;                 // (b, h) pairs whose items run side by side (L2 reuse)
 };
 
 // TMA descriptors of q, k, v and dout for the tensor-core backward.

@@ -21,9 +21,13 @@
 // itself: S and dP are formed in both kernels, which is what keeps dQ free of
 // atomics.  The scale is applied to dK and dQ in the epilogues.
 //
-// Roles (256 threads): warp 0 TMA producer (and the LSE / D rows, loaded by its
+// Roles (384 threads): warp 0 TMA producer (and the LSE / D rows, loaded by its
 // 32 lanes), warp 1 TMEM owner and MMA issuer (converged, one elected lane per
-// instruction), warps 4..7 elementwise + epilogue (thread t owns TMEM lane t).
+// instruction), two elementwise + epilogue groups: warps 4..7 take half 0 and
+// warps 8..11 half 1 of every partner tile (thread t of a group owns TMEM lane
+// t; two warps per sub-partition share the elementwise work of a tile), and
+// split the epilogue (dK/dV: dV rows / dK rows; dQ: the two column halves).
+// Warps 2..3 idle (the groups must start on a warpgroup boundary).
 // Every mbarrier wait is bounded, as in the forward kernel.
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -264,11 +268,11 @@ __device__ __forceinline__ uint32_t bwd_prologue(uint32_t bars, volatile uint32_
             mbar_init(bar(C::B_PFULL + hh), 128);
         }
         mbar_init(bar(C::B_ACCF), 1);
-        mbar_init(bar(C::B_ACCE), 128);   // every elementwise thread after its epilogue
+        mbar_init(bar(C::B_ACCE), 256);   // every elementwise thread (both groups) after its epilogue
         mbar_init(bar(C::B_DRAIN), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::B_ITEMF + i), 1);
-            mbar_init(bar(C::B_ITEME + i), 1 + 4);   // MMA warp + one lane per elementwise warp
+            mbar_init(bar(C::B_ITEME + i), 1 + 8);   // MMA warp + one lane per elementwise warp
         }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -305,9 +309,11 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, l
 // row.  Every lane of the warp executes the (warp-collective) TMEM loads; only
 // lanes with a valid row store.
 template <int D>
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, float *dst, float mul, bool acc, bool valid) {
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float *dst, float mul, bool acc, bool valid,
+                                              int c_begin = 0, int c_end = D / 32) {
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
+        if (c < c_begin || c >= c_end) continue;
         uint32_t r[32];
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
@@ -334,7 +340,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float *dst, float 
 // ---------------------------------------------------------------------------
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dkdv_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo) {
     using C = BCfg<D>;
@@ -557,6 +563,7 @@ __global__ void __launch_bounds__(256, 1)
         // ------------------------------------------------------------ elementwise + epilogue
         const int j = (warp & 3) * 32 + lane;               // key row of the tile (TMEM lane)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const int grp = (warp - 4) >> 2;                    // group: half grp of every partner tile
         const float sl2 = a.scale * 1.4426950408889634f;
         bool ok = true;
         uint32_t t = 0;   // query tiles so far, over all items
@@ -586,7 +593,7 @@ __global__ void __launch_bounds__(256, 1)
                 const bool full = kt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                                   (!a.causal || kt.pos0 + TILE - 1 <= pt.pos0);
 #pragma unroll 1
-                for (int c = 0; c < TILE / 32; ++c) {
+                for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
                     const int hh = c >> 1;   // half of the tile: queries [64 hh, 64 hh + 64)
                     if ((c & 1) == 0) {
                         if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
@@ -645,11 +652,15 @@ __global__ void __launch_bounds__(256, 1)
             }
             tc_fence_after();
             const long long row = ((long long)bh * (a.ring ? a.T : a.Lk) + kt.row0 + j) * D;
+            // group 0 writes the dV rows, group 1 the dK rows
             if (n_done > 0) {   // the same for every lane: the TMEM loads below stay warp-collective
-                store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dv + row, 1.f, a.accumulate != 0, jvalid);
-                store_acc_row<D>(tmem + lane_addr + C::ACC1_COL, a.dk + row, a.scale, a.accumulate != 0, jvalid);
+                if (grp == 0)
+                    store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dv + row, 1.f, a.accumulate != 0, jvalid);
+                else
+                    store_acc_row<D>(tmem + lane_addr + C::ACC1_COL, a.dk + row, a.scale, a.accumulate != 0, jvalid);
             } else if (jvalid && !a.accumulate) {
-                for (int c = 0; c < D; ++c) a.dv[row + c] = a.dk[row + c] = 0.f;
+                float *dst = grp == 0 ? a.dv : a.dk;
+                for (int c = 0; c < D; ++c) dst[row + c] = 0.f;
             }
             tc_fence_before();
             mbar_arrive(bar(C::B_ACCE));
@@ -669,7 +680,7 @@ __global__ void __launch_bounds__(256, 1)
 // ---------------------------------------------------------------------------
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dq_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo) {
     using C = BCfg<D>;
@@ -852,6 +863,7 @@ __global__ void __launch_bounds__(256, 1)
         // ------------------------------------------------------------ elementwise + epilogue
         const int i = (warp & 3) * 32 + lane;               // query row of the tile (TMEM lane)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const int grp = (warp - 4) >> 2;                    // group: half grp of every partner tile
         const float sl2 = a.scale * 1.4426950408889634f;
         bool ok = true;
         uint32_t t = 0;   // key tiles so far, over all items
@@ -886,7 +898,7 @@ __global__ void __launch_bounds__(256, 1)
                 const bool full = qt.len == TILE && pt.len == TILE && !a.kpm && !a.am &&
                                   (!a.causal || pt.pos0 + TILE - 1 <= qt.pos0);
 #pragma unroll 1
-                for (int c = 0; c < TILE / 32; ++c) {
+                for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
                     const int hh = c >> 1;   // half of the tile: keys [64 hh, 64 hh + 64)
                     if ((c & 1) == 0) {
                         if (!warp_wait(bar(C::B_SFULL + hh), t & 1, abort, a.err, lim)) {
@@ -935,10 +947,12 @@ __global__ void __launch_bounds__(256, 1)
             }
             tc_fence_after();
             const long long row = ((long long)bh * q_rows + qt.row0 + i) * D;
+            // group g writes columns [g D/2, g D/2 + D/2) of the dQ rows
             if (n_done > 0)   // uniform: the TMEM loads stay warp-collective
-                store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dq + row, a.scale, a.accumulate != 0, ivalid);
+                store_acc_row<D>(tmem + lane_addr + C::ACC0_COL, a.dq + row, a.scale, a.accumulate != 0, ivalid,
+                                 grp * (D / 64), grp * (D / 64) + D / 64);
             else if (ivalid && !a.accumulate)
-                for (int c = 0; c < D; ++c) a.dq[row + c] = 0.f;
+                for (int c = grp * (D / 2); c < grp * (D / 2) + D / 2; ++c) a.dq[row + c] = 0.f;
             tc_fence_before();
             mbar_arrive(bar(C::B_ACCE));
         }
@@ -974,8 +988,8 @@ int launch_bwd_tc_d(const BwdArgs &a, const BwdMaps &m, int num_sms, cudaStream_
     const long long cap = persistent ? num_sms : 0x7fffffffLL;
     const int g_kv = (int)(n_kt * BH < cap ? n_kt * BH : cap);
     const int g_q = (int)(n_qt * BH < cap ? n_qt * BH : cap);
-    if (g_kv > 0) bwd_dkdv_tc_kernel<D><<<g_kv, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
-    if (g_q > 0) bwd_dq_tc_kernel<D><<<g_q, 256, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    if (g_kv > 0) bwd_dkdv_tc_kernel<D><<<g_kv, 384, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
+    if (g_q > 0) bwd_dq_tc_kernel<D><<<g_q, 384, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.dout);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 

@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller cases for counter captures)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=8, help="head / batch groups pipelined in the e2e leg")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
     ap.add_argument("--seq", type=int, default=None,
                     help="override the workload's sequence length (smaller cases for counter captures)")
@@ -471,7 +472,7 @@ def native_arm(args, w, rank, world, local_rank):
         # streams: host->device copy of group g+1 and device->host copy of group g-1
         # run while group g computes, each group one ring_attn_fwd call, the groups
         # alternating between two compute streams.
-        n_groups = 8
+        n_groups = args.e2e_groups
         if w.B == 1 and w.H % n_groups == 0:
             sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
         elif w.B % n_groups == 0:

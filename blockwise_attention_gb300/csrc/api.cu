@@ -625,11 +625,12 @@ __global__ void __launch_bounds__(256, 3) rope_bf16_kernel(const RopeArgs a) {
 // without registers held for them, and no block-wide barrier is taken per
 // row.  Every wait is bounded: on expiry the thread records the timeout and
 // stops (the streaming thread first lets its copies in flight land).
-constexpr int ROPE_RING = 6;   // 24 KB of slots (even: rows go two by two); three CTAs an SM keep 72 KB in flight
+constexpr int ROPE_RING = 12;   // 48 KB of slots (even: rows go two by two); three CTAs an SM keep 144 KB in flight
 __global__ void __launch_bounds__(256, 3) rope_bf16_bulk_kernel(const RopeArgs a) {
     __shared__ float4 tab[128];
     __shared__ float4 exact[4][256];
-    __shared__ __align__(128) uint4 ring[ROPE_RING][256];
+    extern __shared__ __align__(128) uint4 ring_mem[];   // ROPE_RING slots of 256 16-byte words
+    uint4(*ring)[256] = reinterpret_cast<uint4(*)[256]>(ring_mem);
     __shared__ __align__(8) uint64_t full[ROPE_RING], empty[ROPE_RING];
     __shared__ int abort_flag;
     if (threadIdx.x < 128) tab[threadIdx.x] = a.tab[threadIdx.x];
@@ -910,8 +911,13 @@ int launch_rope(const ba_tensor &x, const ba_tensor *x2, int B, int H, int T, in
         const dim3 grid((unsigned)gx, (unsigned)gy);
         bool rows_contiguous = vec;
         for (int i = 0; i < a.n; ++i) rows_contiguous = rows_contiguous && a.sT[i] == d;
-        if (rows_contiguous)
-            rope_bf16_bulk_kernel<<<grid, threads, 0, s>>>(a);
+        if (rows_contiguous) {
+            const int ring_bytes = ROPE_RING * 256 * 16;
+            if (cudaFuncSetAttribute(rope_bf16_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ring_bytes) !=
+                cudaSuccess)
+                return BA_ERR_CUDA;
+            rope_bf16_bulk_kernel<<<grid, threads, ring_bytes, s>>>(a);
+        }
         else if (vec)
             rope_bf16_kernel<true><<<grid, threads, 0, s>>>(a);
         else

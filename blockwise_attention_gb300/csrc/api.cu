@@ -97,12 +97,12 @@ int zero_sched(void *p, int launches, cudaStream_t s) {
 bool valid_dtype(int t) { return t == BA_F32 || t == BA_BF16; }
 bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
-// (B, H, rows, d) bf16 tensor map: 4-D, box 64 columns x 128 rows, 128B swizzle.
+// (B, H, rows, d) bf16 tensor map: 4-D, box 64 columns x box_rows rows, 128B swizzle.
 int encode_map(CUtensorMap *m, const void *base, int d, long long rows, int H, int B, long long sT, long long sH,
-               long long sB) {
+               long long sB, int box_rows = TILE) {
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)sT * 2, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)TILE, 1, 1};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -113,12 +113,12 @@ int encode_map(CUtensorMap *m, const void *base, int d, long long rows, int H, i
 // Striped ring: the (B, H, T, d) tensor seen as {d, P, T/P, H, B}, token
 // r + P u at coordinates (r, u), so that a box {64, 1, 128, 1, 1} loads 128
 // consecutive tokens of rank r (a stride of P rows) into the same shared-memory
-// layout as the 4-D box.
+// layout as the 4-D box (box_rows consecutive tokens of the rank for the stores).
 int encode_map_striped(CUtensorMap *m, const void *base, int d, int P, long long T, int H, int B, long long sT,
-                       long long sH, long long sB) {
+                       long long sH, long long sB, int box_rows = TILE) {
     cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)P, (cuuint64_t)(T / P), (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[4] = {(cuuint64_t)sT * 2, (cuuint64_t)sT * 2 * P, (cuuint64_t)sH * 2, (cuuint64_t)sB * 2};
-    cuuint32_t box[5] = {64, 1, (cuuint32_t)TILE, 1, 1};
+    cuuint32_t box[5] = {64, 1, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -940,17 +940,24 @@ int run_attention(AttnArgs &a, int dev, int nrows_q, int nrows_k, cudaStream_t s
     int rc = get_encoder();
     if (rc) return rc;
     TmaMaps m;
+    std::memset(&m, 0, sizeof m);
     const int B = a.g.B, H = a.g.H, d = a.g.d;
+    // Full tiles of a bf16 output with nothing to merge are written by TMA stores
+    // (boxes of 32 rows, one per softmax warp); out is (B, H, rows, d) contiguous.
+    const long long osT = d, osH = a.rows * (long long)d, osB = osH * H;
+    a.tma_out = a.out_dtype == BA_BF16 && a.acc_o == nullptr && reinterpret_cast<uintptr_t>(a.out) % 16 == 0;
     if (a.g.striped) {
         const int P = a.g.P;
         if ((rc = encode_map_striped(&m.q, a.q, d, P, nrows_q, H, B, a.qsT, a.qsH, a.qsB))) return rc;
         if ((rc = encode_map_striped(&m.k, a.k, d, P, nrows_k, H, B, a.ksT, a.ksH, a.ksB))) return rc;
         if ((rc = encode_map_striped(&m.v, a.v, d, P, nrows_k, H, B, a.vsT, a.vsH, a.vsB))) return rc;
+        if (a.tma_out && encode_map_striped(&m.o, a.out, d, P, a.rows, H, B, osT, osH, osB, 32)) a.tma_out = 0;
         return launch_attn_tc(a, m, g_num_sms[dev], s);
     }
     if ((rc = encode_map(&m.q, a.q, d, nrows_q, H, B, a.qsT, a.qsH, a.qsB))) return rc;
     if ((rc = encode_map(&m.k, a.k, d, nrows_k, H, B, a.ksT, a.ksH, a.ksB))) return rc;
     if ((rc = encode_map(&m.v, a.v, d, nrows_k, H, B, a.vsT, a.vsH, a.vsB))) return rc;
+    if (a.tma_out && encode_map(&m.o, a.out, d, a.rows, H, B, osT, osH, osB, 32)) a.tma_out = 0;
     return launch_attn_tc(a, m, g_num_sms[dev], s);
 }
 

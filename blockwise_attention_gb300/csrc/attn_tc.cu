@@ -51,7 +51,10 @@
 namespace ba {
 namespace {
 
-template <int D>
+// ST: the layout has the output staging region (instantiations that store
+// full tiles by TMA); without it the shared-memory carve-out stays smaller,
+// which leaves more L1 for the long-walk kernel's spill slots.
+template <int D, bool ST>
 struct Cfg {
     static constexpr int NBOX = D / 64;            // 64-column boxes per tile
     static constexpr int BOX_BYTES = TILE * 128;   // 128 rows x 128 bytes
@@ -62,7 +65,11 @@ struct Cfg {
     static constexpr int Q_OFF = 0;                // query tile x at Q_OFF + x * TILE_BYTES
     static constexpr int K_OFF = 2 * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
-    static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
+    // Output staging: 32 rows x 64 columns (bf16, 128B swizzle) per softmax warp,
+    // warp q of group x at OST_OFF + (4 x + q) * OST_WARP; a TMA store writes them out.
+    static constexpr int OST_WARP = 32 * 128;
+    static constexpr int OST_OFF = V_OFF + VS * TILE_BYTES;
+    static constexpr int BAR_OFF = OST_OFF + (ST ? 8 * OST_WARP : 0);
     enum {
         B_QFULL = 0,
         B_QEMPTY,
@@ -196,8 +203,9 @@ __device__ __noinline__ Keep4 keep_bits4(const Geom &g, int b, long long qpos, b
 template <int D, bool S, bool PF>
 __global__ void __launch_bounds__(320, 1)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tq,
-                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
-    using C = Cfg<D>;
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                   const __grid_constant__ CUtensorMap to) {
+    using C = Cfg<D, PF>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -670,24 +678,77 @@ __global__ void __launch_bounds__(320, 1)
             const long long row_flat = ((long long)qt.b * g.H + qt.h) * a.rows + out_row<S>(g, qt, row);
             const float acc_l = (a.acc_lse != nullptr && valid) ? a.acc_lse[row_flat] : -INFINITY;
             const RowFinal f = row_final(m_ref, n > 0 ? l : 0.f, acc_l);
+            // (the instantiations for long walks keep the per-row stores: there the
+            // item boundary is rare and the staging code costs registers in the loop)
+            if (PF && a.tma_out && qt.len == TILE) {
+                // Full tile, bf16 output, no partial to merge: each warp stages its
+                // 32 rows, 64 columns at a time, in shared memory (128B swizzle: the
+                // 16-byte unit u of row r at unit u ^ (r & 7)) and writes them with one
+                // TMA store, so that the global writes are whole lines and the warp
+                // does not wait for them.
+                const uint32_t ost = base + C::OST_OFF + (uint32_t)(4 * x + quad) * C::OST_WARP;
+                const uint32_t orow = ost + (uint32_t)lane * 128u;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                float o[32];
-                if (n > 0) {
-                    tmem_ld32(tmem + lane_addr + ocol + c * 32, r);
-                    tmem_wait_ld();
+                for (int bx = 0; bx < C::NBOX; ++bx) {
+                    // the staging rows are free once the previous store has read them
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
-                } else {
+                    for (int c = 2 * bx; c < 2 * bx + 2; ++c) {
+                        uint32_t r[32];
+                        if (n > 0) {
+                            tmem_ld32(tmem + lane_addr + ocol + c * 32, r);
+                            tmem_wait_ld();
+                        } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                            for (int i = 0; i < 32; ++i) r[i] = 0u;
+                        }
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; ++u4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                w[k] = pack_bf16(f.wb * (__uint_as_float(r[8 * u4 + 2 * k]) * f.inv_l),
+                                                 f.wb * (__uint_as_float(r[8 * u4 + 2 * k + 1]) * f.inv_l));
+                            const uint32_t u = (uint32_t)(4 * (c & 1) + u4);
+                            st_shared_v4(orow + ((u ^ (uint32_t)(lane & 7)) << 4), w);
+                        }
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (S)
+                            tma_store_5d(&to, ost, bx * 64, qt.rank, (int)qt.pos0 + 32 * quad, qt.h, qt.b);
+                        else
+                            tma_store_4d(&to, ost, bx * 64, qt.row0 + 32 * quad, qt.h, qt.b);
+                        bulk_commit();
+                    }
                 }
-                if (valid) store_row_chunk(a, row_flat, c * 32, o, 32, f);
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    float o[32];
+                    if (n > 0) {
+                        tmem_ld32(tmem + lane_addr + ocol + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    }
+                    if (valid) store_row_chunk(a, row_flat, c * 32, o, 32, f);
+                }
             }
             if (valid) a.lse[row_flat] = f.lse;
             tc_fence_before();
             mbar_arrive(bar(C::B_OEMPTY + x));
+        }
+        if constexpr (PF) {
+            // the output stores this warp issued have finished before the CTA exits
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
         }
     }
 
@@ -702,13 +763,13 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool S, bool PF>
 int launch_dpf(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
-    using C = Cfg<D>;
+    using C = Cfg<D, PF>;
     static_assert(C::SMEM_BYTES <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, S, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
     if (e != cudaSuccess) return BA_ERR_CUDA;
     int grid = a.g.n_items < num_sms ? a.g.n_items : num_sms;
-    attn_tc_kernel<D, S, PF><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v);
+    attn_tc_kernel<D, S, PF><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(a, m.q, m.k, m.v, m.o);
     return cudaGetLastError() == cudaSuccess ? BA_OK : BA_ERR_CUDA;
 }
 
@@ -731,7 +792,7 @@ int launch_d(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
 
 bool tc_supported(int dtype, int d) { return dtype == BA_BF16 && (d == 64 || d == 128); }
 
-size_t tc_smem_bytes(int d) { return d == 128 ? Cfg<128>::SMEM_BYTES : Cfg<64>::SMEM_BYTES; }
+size_t tc_smem_bytes(int d) { return d == 128 ? Cfg<128, true>::SMEM_BYTES : Cfg<64, true>::SMEM_BYTES; }
 
 int launch_attn_tc(const AttnArgs &a, const TmaMaps &m, int num_sms, cudaStream_t s) {
     // The kernel's unit of work is a pair of query tiles (work_pair).

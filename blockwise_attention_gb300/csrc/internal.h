@@ -20,6 +20,7 @@ struct AttnArgs {
     float scale_log2;                    // softmax scale * log2(e)
     void *out;                           // (B, H, rows, d) contiguous, out_dtype
     int out_dtype;
+    int tma_out;                         // tensor-core kernel: full tiles stored by TMA (map `o`)
     float *lse;                          // (B, H, rows) natural-log LSE
     long long rows;                      // rows of out/lse per (b, h): Lq or T
     const float *acc_o;                  // nullable fp32 (B, H, rows, d) partial to merge with
@@ -102,9 +103,10 @@ struct DecodeArgs {
 
 int launch_decode(const DecodeArgs &a, cudaStream_t s);
 
-// TMA descriptors of Q, K, V for the tensor-core kernel.
+// TMA descriptors of Q, K, V (loads) and out (stores, boxes of 32 rows) for
+// the tensor-core kernel.
 struct TmaMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 int launch_attn_simt(const AttnArgs &a, cudaStream_t s);

@@ -252,3 +252,40 @@ def test_growing_scores_rescale(d, causal, ring):
     s_last = (q.float()[0, 0, -1] @ k.float()[0, 0].T) / math.sqrt(d) * 1.4426950408889634
     assert float(s_last[-128:].max() - s_last[:128].max()) > 2 * 8.0
     compare(out, lse, o_ref, l_ref, "bf16", f"growing scores d={d} causal={causal} ring={ring}")
+
+
+# Score levels (exp2 units) of the keys of tile t, half h (64 keys each), for
+# rescale_inside_tile: each places a jump where one branch of the tensor-core
+# kernel's lazy rescale runs.  With the reference maximum m of the row taken on
+# the first tile, a later half whose scores sit near m passes on the sum of its
+# p; a half whose scores are 10 above m moves m (more than 2^8 above it), and
+# one 4 above m has a sum of p over 2^8 but moves nothing.
+LEVELS = {
+    "first_half": lambda t, h: 10.0 * t,            # the jump at the start of each tile
+    "second_half": lambda t, h: 10.0 * (t + h),     # the jump in the middle of each tile
+    "sum_only_first": lambda t, h: 4.0 * t,
+    "sum_only_second": lambda t, h: 4.0 * (t + h),
+}
+
+
+@pytest.mark.parametrize("case", sorted(LEVELS))
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_inside_tile(case, d, causal):
+    """Online softmax (brunomaga "Improving numerical stability"): the running
+    maximum of a row moves inside a key tile, in its first or its second half of
+    64 keys, or a half's probabilities sum past 2^8 with the maximum unmoved.
+    The output must match the oracle whichever way the kernel splits the tile."""
+    B, H, T = 1, 2, 384
+    g = torch.Generator(device="cpu").manual_seed(91)
+    q = torch.randn((B, H, T, d), generator=g) * 0.5
+    k = torch.randn((B, H, T, d), generator=g) * 0.5
+    v = torch.randn((B, H, T, d), generator=g)
+    per_unit = 4.0 / math.sqrt(d) * 1.4426950408889634   # exp2 units of score per unit of k[..., 0]
+    q[..., 0] = 4.0
+    lev = torch.tensor([LEVELS[case](j // 128, (j % 128) // 64) for j in range(T)])
+    k[..., 0] = (lev / per_unit).view(1, 1, T)
+    q, k, v = (x.to(torch.bfloat16).cuda() for x in (q, k, v))
+    out, lse = ba.attn_block_fwd(q, k, v, causal=causal, out_dtype=torch.float32)
+    o_ref, l_ref = oracle.attention(q.float().cpu(), k.float().cpu(), v.float().cpu(), causal=causal)
+    compare(out, lse, o_ref, l_ref, "bf16", f"rescale inside tile {case} d={d} causal={causal}")

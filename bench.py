@@ -50,6 +50,9 @@ def parse():
                     help="override the workload's head count (smaller cases for counter captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=8, help="head / batch groups pipelined in the e2e leg")
+    ap.add_argument("--e2e-split", default=None,
+                    help="heads per group of the e2e leg, comma-separated (B = 1; overrides --e2e-groups); "
+                         "default for B = 1 and H a multiple of 16: H/16, 3H/16, H/4, H/4, 3H/16, H/16")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA graph replays")
     ap.add_argument("--seq", type=int, default=None,
                     help="override the workload's sequence length (smaller cases for counter captures)")
@@ -473,7 +476,21 @@ def native_arm(args, w, rank, world, local_rank):
         # run while group g computes, each group one ring_attn_fwd call, the groups
         # alternating between two compute streams.
         n_groups = args.e2e_groups
-        if w.B == 1 and w.H % n_groups == 0:
+        # Small first and last groups: the first group's inputs and the last group's
+        # outputs cross the host link while nothing else runs.
+        if args.e2e_split:
+            split = [int(x) for x in args.e2e_split.split(",")]
+        elif w.B == 1 and w.H % 16 == 0 and args.e2e_groups == 8:
+            u = w.H // 16
+            split = [u, 3 * u, 4 * u, 4 * u, 3 * u, u]
+        else:
+            split = None
+        if split and w.B == 1 and sum(split) == w.H and min(split) > 0:
+            n_groups, edges = len(split), [0]
+            for x in split:
+                edges.append(edges[-1] + x)
+            sl = [(slice(None), slice(edges[i], edges[i + 1])) for i in range(n_groups)]
+        elif w.B == 1 and w.H % n_groups == 0:
             sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
         elif w.B % n_groups == 0:
             sl = [(slice(i * w.B // n_groups, (i + 1) * w.B // n_groups),) for i in range(n_groups)]
@@ -531,6 +548,8 @@ def native_arm(args, w, rank, world, local_rank):
         d2h = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "pipeline_groups": n_groups}
+        if split and n_groups == len(split):
+            e2e["heads_per_group"] = split
         del qh, kh, vh, qd, kd, vd, wse
 
     if ba.sync_status() != 0:

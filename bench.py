@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
     ap.add_argument("--partition", default=None, choices=["contiguous", "zigzag", "striped"],
                     help="override the workload's partition of the P ranks")
+    ap.add_argument("--shard", default=None, choices=["heads"],
+                    help="N > 1: split the workload's heads over the ranks (strong scaling) instead of one "
+                         "replica of the whole workload per rank (weak scaling, the default)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's head count (smaller cases for counter captures)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -159,6 +162,18 @@ def tensor_roofline(achieved, peaks, peak_src, clocks, timed_s):
             "tensor_peak_at_clock": at_clock, "frac_of_peak_at_clock": achieved / at_clock,
             "peak_at_clock_source": f"{TENSOR_FLOP_PER_CLK_SM} FLOP/clk/SM x {NUM_SMS} SMs x median SM clock "
                                     f"{mhz:.0f} MHz"}
+
+
+def shard_heads(H: int, world: int, rank: int):
+    """Heads [h0, h1) of rank `rank` when the H heads of one workload are split
+    over `world` ranks: contiguous, as even as possible (the first H % world ranks
+    take one more).  Heads are independent problems, so no data moves between
+    ranks."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    base, extra = divmod(H, world)
+    h0 = rank * base + min(rank, extra)
+    return h0, h0 + base + (1 if rank < extra else 0)
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -571,15 +586,22 @@ def native_arm(args, w, rank, world, local_rank):
             cpu = oracle_cpu_baseline(w, head, args.cpu_seconds,
                                       kpm=None if inp.kpm is None else inp.kpm[0:1].cpu(),
                                       am=None if inp.am is None else inp.am.cpu())
+    # --shard heads: the ranks together process one workload (value: its FLOPs over
+    # the slowest rank's time); otherwise each rank processes a whole replica
+    sharded = getattr(args, "shard", None) == "heads" and world > 1
+    full = getattr(args, "full_workload", w)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "strong" if sharded else "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "P": w.P,
+            "config": {"workload": full.name if sharded else w.name, "B": w.B, "H": full.H if sharded else w.H,
+                       "T": w.T, "d": w.d, "P": w.P,
+                       "parallelism": f"heads split over {world} ranks" if sharded else f"{world} replica(s)",
                        "partition": w.partition, "causal": w.causal, "rope_base": w.rope_base,
                        "mode": args.mode, "visible_pairs": pairs, "flops_per_step": flops,
                        "launch": "CUDA graph replay" if graphs else "eager",
                        "l2": "inputs (Q, K, V: 1.6 GB) larger than the 129 MB L2; no flush"},
-            "tokens_per_s": world * w.B * w.T / (ms_step * 1e-3),
+            "tokens_per_s": (1 if sharded else world) * w.B * w.T / (ms_step * 1e-3),
             "pct_of_bf16_peak": 100.0 * value / roof["peak"],
             "rope_ms": statistics.mean(rope_ms),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
@@ -961,6 +983,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    args.full_workload = w
+    if args.shard == "heads" and world > 1:
+        if w.H % world:
+            raise SystemExit(f"--shard heads: {w.H} heads do not split evenly over {world} ranks")
+        h0, h1 = shard_heads(w.H, world, rank)
+        # this rank's heads only (synthetic inputs of that shape, seeded per rank)
+        w = w.replace(H=h1 - h0, index=w.index + 7919 * rank, name=f"{w.name}_heads{h0}-{h1}")
     if args.impl == "reference":
         reference_arm(args, w, rank, world)
         return

@@ -54,3 +54,44 @@ def test_traffic_record_matches_sources():
     t = bench.profiled_traffic("zigzag_prefill_64k_rope")
     assert t is None or t > 10**9
     assert bench.profiled_traffic("no_such_workload") is None
+
+
+def _shard_main(rank, world, port, H, results):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        h0, h1 = bench.shard_heads(H, world, rank)
+        # every rank learns every rank's range: they must tile [0, H) with no overlap
+        ranges = [None] * world
+        dist.all_gather_object(ranges, (h0, h1))
+        results[rank] = ranges
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("H,world", [(32, 2), (7, 2)])
+def test_shard_heads_gloo_tiles_the_heads(H, world):
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_main, args=(r, world, port, H, results)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    ranges = results[0]
+    assert all(results[r] == ranges for r in range(world))
+    assert ranges[0][0] == 0 and ranges[-1][1] == H
+    assert all(ranges[i][1] == ranges[i + 1][0] for i in range(world - 1))
+    sizes = [b - a for a, b in ranges]
+    assert max(sizes) - min(sizes) <= 1
+
+
+def test_shard_heads_single_process_cases():
+    assert bench.shard_heads(32, 1, 0) == (0, 32)
+    assert [bench.shard_heads(10, 4, r) for r in range(4)] == [(0, 3), (3, 6), (6, 8), (8, 10)]
+    with pytest.raises(ValueError):
+        bench.shard_heads(8, 2, 2)

@@ -322,6 +322,19 @@ __global__ void __launch_bounds__(320, 1)
                 int prev_row = -1;   // k/v row of the tile whose V is still to be loaded
                 for (;;) {
                     const bool more = pair_next<S>(g, p, wk, kt, c0, c1);
+                    // V of the previous tile first: its products come before this tile's scores
+                    if (prev_row >= 0) {
+                        const uint32_t st = vfill % C::VS, use = vfill / C::VS;
+                        if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
+                        for (int bx = 0; bx < C::NBOX; ++bx)
+                            tma_load_rows<S>(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, g, bx * 64, prev_row,
+                                          p.q0.h, p.q0.b, bar(C::B_VFULL + st));
+                        ++vfill;
+                    }
                     if (more) {
                         const uint32_t st = kfill % C::KS, use = kfill / C::KS;
                         if (use > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
@@ -343,18 +356,6 @@ __global__ void __launch_bounds__(320, 1)
                             tma_load_rows<S>(sK + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tk, g, bx * 64, kt.row0,
                                           p.q0.h, p.q0.b, bar(C::B_KFULL + st));
                         ++kfill;
-                    }
-                    if (prev_row >= 0) {
-                        const uint32_t st = vfill % C::VS, use = vfill / C::VS;
-                        if (use > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (use - 1) & 1, abort, a.err, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE_BYTES);
-                        for (int bx = 0; bx < C::NBOX; ++bx)
-                            tma_load_rows<S>(sV + st * C::TILE_BYTES + bx * C::BOX_BYTES, &tv, g, bx * 64, prev_row,
-                                          p.q0.h, p.q0.b, bar(C::B_VFULL + st));
-                        ++vfill;
                     }
                     if (!more) break;
                     prev_row = kt.row0;

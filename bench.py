@@ -164,6 +164,28 @@ def tensor_roofline(achieved, peaks, peak_src, clocks, timed_s):
                                     f"{mhz:.0f} MHz"}
 
 
+def e2e_groups(B: int, H: int, n_groups: int = 8, split=None):
+    """Index tuples of the groups the e2e leg pipelines, one ring_attn_fwd call
+    each.  B = 1: groups of heads, by default H/16, 3H/16, H/4, H/4, 3H/16, H/16
+    when H is a multiple of 16 and eight groups are asked for (small first and
+    last groups: the first group's inputs and the last group's outputs cross the
+    host link while nothing else runs), else `split` (heads per group) or n_groups
+    equal groups.  Otherwise groups of batch items, or the whole tensor."""
+    if split is None and B == 1 and H % 16 == 0 and n_groups == 8:
+        u = H // 16
+        split = [u, 3 * u, 4 * u, 4 * u, 3 * u, u]
+    if split and B == 1 and sum(split) == H and min(split) > 0:
+        edges = [0]
+        for x in split:
+            edges.append(edges[-1] + x)
+        return [(slice(None), slice(edges[i], edges[i + 1])) for i in range(len(split))]
+    if B == 1 and H % n_groups == 0:
+        return [(slice(None), slice(i * H // n_groups, (i + 1) * H // n_groups)) for i in range(n_groups)]
+    if B % n_groups == 0:
+        return [(slice(i * B // n_groups, (i + 1) * B // n_groups),) for i in range(n_groups)]
+    return [(slice(None),)]
+
+
 def shard_heads(H: int, world: int, rank: int):
     """Heads [h0, h1) of rank `rank` when the H heads of one workload are split
     over `world` ranks: contiguous, as even as possible (the first H % world ranks
@@ -490,27 +512,10 @@ def native_arm(args, w, rank, world, local_rank):
         # streams: host->device copy of group g+1 and device->host copy of group g-1
         # run while group g computes, each group one ring_attn_fwd call, the groups
         # alternating between two compute streams.
-        n_groups = args.e2e_groups
-        # Small first and last groups: the first group's inputs and the last group's
-        # outputs cross the host link while nothing else runs.
-        if args.e2e_split:
-            split = [int(x) for x in args.e2e_split.split(",")]
-        elif w.B == 1 and w.H % 16 == 0 and args.e2e_groups == 8:
-            u = w.H // 16
-            split = [u, 3 * u, 4 * u, 4 * u, 3 * u, u]
-        else:
-            split = None
-        if split and w.B == 1 and sum(split) == w.H and min(split) > 0:
-            n_groups, edges = len(split), [0]
-            for x in split:
-                edges.append(edges[-1] + x)
-            sl = [(slice(None), slice(edges[i], edges[i + 1])) for i in range(n_groups)]
-        elif w.B == 1 and w.H % n_groups == 0:
-            sl = [(slice(None), slice(i * w.H // n_groups, (i + 1) * w.H // n_groups)) for i in range(n_groups)]
-        elif w.B % n_groups == 0:
-            sl = [(slice(i * w.B // n_groups, (i + 1) * w.B // n_groups),) for i in range(n_groups)]
-        else:
-            n_groups, sl = 1, [(slice(None),)]
+        split = [int(x) for x in args.e2e_split.split(",")] if args.e2e_split else None
+        sl = e2e_groups(w.B, w.H, args.e2e_groups, split)
+        n_groups = len(sl)
+        heads_per_group = [ix[1].stop - ix[1].start for ix in sl] if w.B == 1 and len(sl[0]) == 2 else None
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         s_comp = [stream, torch.cuda.Stream(dev)]
         ev_in = [torch.cuda.Event() for _ in range(n_groups)]
@@ -563,8 +568,8 @@ def native_arm(args, w, rank, world, local_rank):
         d2h = oh.numel() * oh.element_size() + lh.numel() * 4
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "pipeline_groups": n_groups}
-        if split and n_groups == len(split):
-            e2e["heads_per_group"] = split
+        if heads_per_group:
+            e2e["heads_per_group"] = heads_per_group
         del qh, kh, vh, qd, kd, vd, wse
 
     if ba.sync_status() != 0:

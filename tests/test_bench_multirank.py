@@ -95,3 +95,18 @@ def test_shard_heads_single_process_cases():
     assert [bench.shard_heads(10, 4, r) for r in range(4)] == [(0, 3), (3, 6), (6, 8), (8, 10)]
     with pytest.raises(ValueError):
         bench.shard_heads(8, 2, 2)
+
+
+def test_e2e_groups_split_heads():
+    def heads(sl):
+        return [(ix[1].start, ix[1].stop) for ix in sl]
+    # default at 32 heads: small first and last groups, tiling [0, 32)
+    assert heads(bench.e2e_groups(1, 32)) == [(0, 2), (2, 8), (8, 16), (16, 24), (24, 30), (30, 32)]
+    # an explicit split, and equal groups when asked for another count
+    assert heads(bench.e2e_groups(1, 32, 8, [4, 8, 8, 8, 4])) == [(0, 4), (4, 12), (12, 20), (20, 28), (28, 32)]
+    assert heads(bench.e2e_groups(1, 32, 4)) == [(0, 8), (8, 16), (16, 24), (24, 32)]
+    # a split that does not cover the heads is ignored
+    assert heads(bench.e2e_groups(1, 32, 8, [4, 4])) == heads(bench.e2e_groups(1, 32, 8))
+    # batch groups, or the whole tensor
+    assert bench.e2e_groups(16, 8, 8) == [(slice(2 * i, 2 * i + 2),) for i in range(8)]
+    assert bench.e2e_groups(4, 16, 8) == [(slice(None),)]
